@@ -1,0 +1,180 @@
+/*
+ * evoattn.h -- C ABI of the GB300 (sm_103a) EvoAttention library.
+ *
+ * EvoAttention is the memory-efficient 3D attention over the 2D pair
+ * representation that MegaFold calls EvoFlash-3D (MegaFold: Efficient
+ * Training of Next-Generation 3D Attention Protein Models on Cross-Platform
+ * GPUs; technical summary, "Methodik" section 1 "EvoFlash-3D": the logits are
+ * produced tile by tile in on-chip memory with an online, numerically stable
+ * softmax in both the forward and the backward pass, never materialising the
+ * O(N^3) attention map in HBM, and carry an additively broadcast pair-bias
+ * term).  Successive layers alternate the attention axis, row-wise then
+ * column-wise (same page, "Methodik" section 2 "EvoSP-3D", Kommunikation);
+ * the column-wise (ending-node) layer is expressed here as strides, not as a
+ * copy.
+ *
+ * For every batch b, row s in [0,S) and head h, with query row j and key k in
+ * [0,N) and feature d in [0,D):
+ *
+ *   x[j,k]   = sum_d q[b,s,h,j,d] k[b,s,h,k,d] / sqrt(D)
+ *              + pair_bias[b,h,j,k] + (mask[b,s,k] ? 0 : -1e9)
+ *   lse[j]   = log sum_k exp(x[j,k])                        (natural log)
+ *   O[j,d]   = sum_k exp(x[j,k] - lse[j]) v[b,s,h,k,d]
+ *   out      = sigmoid(gate) * O     (elementwise; out = O when gate is NULL)
+ *
+ * The pair bias is shared by all S rows (triangle attention around the
+ * starting or ending node: S = N; MSA-row attention with pair bias: S = MSA
+ * depth).  The backward returns dq, dk, dv, dgate and
+ *
+ *   dbias[b,h,j,k] = sum_s dlogits[b,s,h,j,k]
+ *
+ * CONVENTIONS (all entry points)
+ *  - Ownership: the caller owns every buffer.  Device pointers point to
+ *    device memory of the current CUDA device; the library keeps no state
+ *    between calls except one 4-byte device status word per device (see
+ *    evoattn_get_device_status) and the cached driver entry point used to
+ *    build tensor maps.  It never allocates device memory.
+ *  - Execution: work is enqueued on `stream` (a cudaStream_t; 0 = legacy
+ *    default stream) and the call returns without synchronising, except
+ *    evoattn_get_device_status.  Calls on different streams may run
+ *    concurrently when their outputs and workspaces do not overlap.
+ *  - Errors: arguments are validated on the host before anything is
+ *    enqueued; a failing call returns a non-zero evoattn_status and enqueues
+ *    nothing.  A launch failure returns EVOATTN_ERR_CUDA.  The library never
+ *    aborts the process.
+ *  - Shapes: B, S, H, N >= 1.  BF16: D in {16, 32, 64}.  F32: D in
+ *    {16, 32, 64, 128}.
+ *  - Strides are in ELEMENTS (not bytes), one per logical axis, for the
+ *    logical shapes:  q/k/v/gate/out/dout/dq/dk/dv/dgate  [B,S,H,N,D]  as
+ *    {b, s, h, n, d};  pair_bias [B,H,N,N] as {b, h, j, k};  mask [B,S,N] as
+ *    {b, s, k}.  Any non-negative strides are accepted for F32.  For BF16 the
+ *    d stride must be 1, every other stride of a [B,S,H,N,D] tensor a
+ *    multiple of 8 elements (16 bytes), the base address 16-byte aligned;
+ *    the pair bias needs a unit stride along k or along j and its other
+ *    strides multiples of 8 elements.  Otherwise EVOATTN_ERR_ALIGNMENT.
+ *  - mask is uint8, nonzero = keep; NULL means every key is kept.  A row
+ *    whose keys are all masked yields a uniform softmax over its keys (every
+ *    logit saturates at -1e9 in fp32).
+ *  - The forward writes lse as fp32 [B,S,H,N] contiguous; the backward reads
+ *    it in the same layout.
+ *  - BF16 inputs produce BF16 out/dq/dk/dv/dgate; dbias and lse are always
+ *    fp32.  F32 inputs produce F32 outputs.
+ */
+#ifndef EVOATTN_H
+#define EVOATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EVOATTN_OK = 0,
+    EVOATTN_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad flag */
+    EVOATTN_ERR_UNSUPPORTED = 2,   /* D or dtype outside the supported set */
+    EVOATTN_ERR_ALIGNMENT = 3,     /* stride / address rule of the BF16 path broken */
+    EVOATTN_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than required */
+    EVOATTN_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+    EVOATTN_ERR_TIMEOUT = 6        /* a kernel gave up a bounded wait (device status) */
+} evoattn_status;
+
+typedef enum { EVOATTN_BF16 = 0, EVOATTN_F32 = 1 } evoattn_dtype;
+
+/* evoattn_bwd flags */
+#define EVOATTN_DBIAS_DETERMINISTIC 0u  /* fixed s-slots + ordered sum: bit-identical */
+#define EVOATTN_DBIAS_ATOMIC 1u         /* s-slot partials added with fp32 atomics */
+
+/*
+ * Forward (MegaFold technical summary, "Methodik" section 1 "EvoFlash-3D",
+ * Mechanismus and Optimierung).
+ *
+ *  q, k, v, gate : [B,S,H,N,D] device, dtype `dtype`; gate may be NULL.
+ *  pair_bias     : [B,H,N,N] device, dtype `dtype` (indexed [b,h,j,k]).
+ *  mask          : [B,S,N] device uint8 or NULL (then mask_strides is ignored).
+ *  out           : [B,S,H,N,D] device, written.
+ *  lse           : [B,S,H,N] device fp32 contiguous, written (natural log of
+ *                  the softmax normaliser of each query row, as in x above).
+ *  *_strides     : host arrays, element strides as in CONVENTIONS.
+ * Returns EVOATTN_OK once the kernels are enqueued.
+ */
+evoattn_status evoattn_fwd(const void* q, const int64_t q_strides[5],
+                           const void* k, const int64_t k_strides[5],
+                           const void* v, const int64_t v_strides[5],
+                           const void* pair_bias, const int64_t bias_strides[4],
+                           const uint8_t* mask, const int64_t mask_strides[3],
+                           const void* gate, const int64_t gate_strides[5],
+                           void* out, const int64_t out_strides[5],
+                           float* lse,
+                           int B, int S, int H, int N, int D,
+                           evoattn_dtype dtype, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace evoattn_bwd needs for this problem (0 on invalid
+ * sizes).  Linear in B*S*H*N*D plus O(B*H*N*N) for the dbias partial sums;
+ * never proportional to B*S*H*N*N.
+ */
+size_t evoattn_bwd_workspace_size(int B, int S, int H, int N, int D,
+                                  evoattn_dtype dtype, unsigned flags);
+
+/*
+ * Backward (same section: the logits are recomputed tile by tile in the
+ * backward pass as well).
+ *
+ *  q..gate, pair_bias, mask : as passed to evoattn_fwd.
+ *  out, lse                 : the forward's outputs for these inputs.
+ *  dout                     : [B,S,H,N,D] device, gradient of the loss w.r.t. out.
+ *  dq, dk, dv               : [B,S,H,N,D] device, written.
+ *  dbias                    : [B,H,N,N] device fp32 contiguous, written (the
+ *                             sum over s of the logit gradients).
+ *  dgate                    : [B,S,H,N,D] device, written; must be NULL
+ *                             exactly when gate is NULL.
+ *  flags                    : EVOATTN_DBIAS_DETERMINISTIC (bit-identical
+ *                             dbias from run to run and box to box) or
+ *                             EVOATTN_DBIAS_ATOMIC (same partials combined
+ *                             with atomics; order-dependent rounding).
+ *  workspace                : device, 256-byte aligned, at least
+ *                             evoattn_bwd_workspace_size(...) bytes; the
+ *                             library overwrites it; it must not be used by
+ *                             another call that runs concurrently.
+ */
+evoattn_status evoattn_bwd(const void* q, const int64_t q_strides[5],
+                           const void* k, const int64_t k_strides[5],
+                           const void* v, const int64_t v_strides[5],
+                           const void* pair_bias, const int64_t bias_strides[4],
+                           const uint8_t* mask, const int64_t mask_strides[3],
+                           const void* gate, const int64_t gate_strides[5],
+                           const void* out, const int64_t out_strides[5],
+                           const float* lse,
+                           const void* dout, const int64_t dout_strides[5],
+                           void* dq, const int64_t dq_strides[5],
+                           void* dk, const int64_t dk_strides[5],
+                           void* dv, const int64_t dv_strides[5],
+                           float* dbias,
+                           void* dgate, const int64_t dgate_strides[5],
+                           int B, int S, int H, int N, int D,
+                           evoattn_dtype dtype, unsigned flags,
+                           void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the calling device's status
+ * word.  *device_status receives EVOATTN_OK, or EVOATTN_ERR_TIMEOUT when a
+ * kernel enqueued since the last read gave up a bounded wait (its outputs are
+ * then undefined).  Returns EVOATTN_ERR_CUDA if synchronising or the copy
+ * fails, EVOATTN_ERR_INVALID_ARG if device_status is NULL.
+ */
+evoattn_status evoattn_get_device_status(cudaStream_t stream, int* device_status);
+
+/* Static, NUL-terminated English description of a status code. */
+const char* evoattn_status_string(evoattn_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int evoattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EVOATTN_H */

@@ -1,0 +1,497 @@
+// EvoAttention forward on sm_103a: TMA-fed tcgen05 MMAs with TMEM
+// accumulators and an online softmax in registers.
+//
+// MegaFold technical summary, "Methodik" section 1 "EvoFlash-3D": the logits
+// of one query tile against one key tile are produced in on-chip memory and
+// folded into a running (max, sum) pair -- the online normalizer of softmax --
+// so the B*S*H*N*N attention map never reaches HBM; the pair bias, broadcast
+// over the S rows, is added to every logit tile.
+//
+// CTA = one (b, h, 128-row query tile jt) and a group of G consecutive rows s.
+// The key tiles kt form the outer loop and the G rows the inner loop, so each
+// 128x128 pair-bias tile is loaded into shared memory once and serves G rows.
+//
+// Warp roles (320 threads):
+//   warp 0      TMA producer: Q tiles, the bias tile of each kt, K/V tiles of
+//               each (kt, s) and the additive key mask of that (s, kt)
+//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM, O += P V with
+//               P read from TMEM
+//   warps 2-5   softmax warpgroup 0: rows s = 0, 2, ... of the group
+//   warps 6-9   softmax warpgroup 1: rows s = 1, 3, ...
+// A softmax thread owns one query row j (TMEM lane 32*(warp%4) + lane).
+//
+// Tensor memory (512 columns): S buffer of warpgroup w at columns 128*w (fp32
+// 128x128; the bf16 P overwrites its first 64 columns), O of row s at
+// 256 + s*D (fp32 128xD).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "layout.cuh"
+#include "sm103.h"
+#include "tmap.h"
+
+namespace evo {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128;                   // query rows per tile
+  static constexpr int BN = 128;                   // keys per tile
+  static constexpr int G = (D == 64) ? 2 : 4;      // rows s per CTA
+  static constexpr int NS = 3;                     // K/V pipeline stages
+  static constexpr uint32_t ROW = D * 2;           // bytes of one bf16 row
+  static constexpr uint32_t ATOM = 8 * ROW;        // swizzle atom (8 rows)
+  static constexpr Swizzle SW = D == 16 ? kSw32 : (D == 32 ? kSw64 : kSw128);
+  static constexpr uint32_t TILE = 128 * ROW;      // one 128-row Q/K/V tile
+  static constexpr uint32_t BIAS_TILE = 128 * 128 * 2;
+  // shared memory carve-up (offsets from a 1024-aligned base)
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + G * TILE;
+  static constexpr uint32_t OFF_V = OFF_K + NS * TILE;
+  static constexpr uint32_t OFF_BIAS = OFF_V + NS * TILE;
+  static constexpr uint32_t OFF_MADD = OFF_BIAS + 2 * BIAS_TILE;
+  static constexpr uint32_t SMEM = OFF_MADD + NS * BN * 4;
+  static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TMEM_O = 256;
+  static constexpr int THREADS = 320;
+};
+
+struct FwdParams {
+  int B, S, H, N;
+  int n_jt, n_kt, n_sg;
+  const unsigned char* mask;
+  int64_t msb, mss, msk;
+  const __nv_bfloat16* gate;
+  Strides5 g;
+  __nv_bfloat16* out;
+  Strides5 o;
+  float* lse;
+  unsigned int* status;
+};
+
+template <int D, bool BIAS_K_CONTIG, bool HAS_GATE>
+__global__ void __launch_bounds__(320, 1)
+    evoattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_bias, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bar_q, bar_kv_full[C::NS], bar_kv_empty[C::NS], bar_bias_full[2],
+      bar_bias_empty[2], bar_s_full[2], bar_p_ready[2], bar_o_done[C::G], bar_drain;
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag;
+
+  // ---- tile coordinates -------------------------------------------------
+  int idx = blockIdx.x;
+  const int jt = idx % p.n_jt; idx /= p.n_jt;
+  const int h = idx % p.H; idx /= p.H;
+  const int sg = idx % p.n_sg;
+  const int b = idx / p.n_sg;
+  const int s0 = sg * C::G;
+  const int g_eff = min(C::G, p.S - s0);
+  const int nkt = p.n_kt;
+  const int total = nkt * g_eff;
+  const int n_wg = g_eff >= 2 ? 2 : 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_q, 1);
+    for (int i = 0; i < C::NS; ++i) { mbar_init(&bar_kv_full[i], 1); mbar_init(&bar_kv_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_bias_full[i], 1);
+      mbar_init(&bar_bias_empty[i], 128 * n_wg);
+      mbar_init(&bar_s_full[i], 1);
+      mbar_init(&bar_p_ready[i], 128);
+    }
+    for (int i = 0; i < C::G; ++i) mbar_init(&bar_o_done[i], 1);
+    mbar_init(&bar_drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_base_slot, C::TMEM_COLS);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v); tma_prefetch_desc(&tm_bias);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_slot;
+  volatile int* abort_p = &abort_flag;
+
+  if (warp == 0) {
+    // =================== TMA producer (whole warp) ========================
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar_q, g_eff * C::TILE);
+      for (int s = 0; s < g_eff; ++s)
+        tma_load_5d(smem + C::OFF_Q + s * C::TILE, &tm_q, &bar_q, 0, jt * C::BM, h, s0 + s, b);
+    }
+    bool ok = true;
+    int kv_issued = 0, bias_issued = 0;  // fills issued so far
+    for (int kt = 0; kt < nkt && ok; ++kt) {
+      const int bs = kt & 1;
+      if (kt >= 2) ok = mbar_wait(&bar_bias_empty[bs], ((kt >> 1) - 1) & 1, abort_p);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      if (lane == 0) {
+        uint8_t* dst = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
+        mbar_arrive_expect_tx(&bar_bias_full[bs], C::BIAS_TILE);
+        if (BIAS_K_CONTIG) {
+          tma_load_4d(dst, &tm_bias, &bar_bias_full[bs], kt * C::BN, jt * C::BM, h, b);
+          tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, &bar_bias_full[bs], kt * C::BN + 64,
+                      jt * C::BM, h, b);
+        } else {
+          tma_load_4d(dst, &tm_bias, &bar_bias_full[bs], jt * C::BM, kt * C::BN, h, b);
+          tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, &bar_bias_full[bs], jt * C::BM + 64,
+                      kt * C::BN, h, b);
+        }
+      }
+      bias_issued = kt + 1;
+      for (int s = 0; s < g_eff; ++s) {
+        const int i = kt * g_eff + s;
+        const int st = i % C::NS;
+        if (i >= C::NS) ok = mbar_wait(&bar_kv_empty[st], ((i / C::NS) - 1) & 1, abort_p);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        // additive key mask of (s, kt) in log2 units: 0 kept, -1e9*log2(e)
+        // masked, -inf beyond N
+        float* madd = reinterpret_cast<float*>(smem + C::OFF_MADD + st * C::BN * 4);
+        const unsigned char* mrow =
+            p.mask ? p.mask + b * p.msb + (int64_t)(s0 + s) * p.mss : nullptr;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kk = kt * C::BN + e * 32 + lane;
+          float a = 0.f;
+          if (kk >= p.N) a = -INFINITY;
+          else if (mrow && !mrow[kk * p.msk]) a = kMaskBias * kLog2e;
+          madd[e * 32 + lane] = a;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_kv_full[st], 2 * C::TILE);
+          tma_load_5d(smem + C::OFF_K + st * C::TILE, &tm_k, &bar_kv_full[st], 0, kt * C::BN, h,
+                      s0 + s, b);
+          tma_load_5d(smem + C::OFF_V + st * C::TILE, &tm_v, &bar_kv_full[st], 0, kt * C::BN, h,
+                      s0 + s, b);
+        }
+        kv_issued = i + 1;
+      }
+    }
+    // After a give-up, let every copy already issued land before the CTA may
+    // exit (those waits end by themselves: a copy does not depend on the
+    // other roles).
+    if (!ok && lane == 0) {
+      volatile int no_abort = 0;
+      for (int i = max(0, kv_issued - C::NS); i < kv_issued; ++i)
+        mbar_wait(&bar_kv_full[i % C::NS], (i / C::NS) & 1, &no_abort);
+      for (int kt = max(0, bias_issued - 2); kt < bias_issued; ++kt)
+        mbar_wait(&bar_bias_full[kt & 1], (kt >> 1) & 1, &no_abort);
+      mbar_wait(&bar_q, 0, &no_abort);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // =================== MMA issuer ========================================
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q, K both K-major
+      constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);    // P from TMEM, V MN-major
+      const uint32_t sq = smem_u32(smem + C::OFF_Q), sk = smem_u32(smem + C::OFF_K),
+                     sv = smem_u32(smem + C::OFF_V);
+      bool ok = mbar_wait(&bar_q, 0, abort_p);
+      auto issue_qk = [&](int i) -> bool {
+        const int s = i % g_eff, st = i % C::NS, w = s & 1;
+        if (!mbar_wait(&bar_kv_full[st], (i / C::NS) & 1, abort_p)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + 128 * w, umma_desc(sq + s * C::TILE + kk * 32, 16, C::ATOM, C::SW),
+                  umma_desc(sk + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_s, kk > 0);
+        umma_commit(&bar_s_full[w]);
+        return true;
+      };
+      // first S tile of each warpgroup
+      int wg_iter[2] = {0, 0};
+      if (ok) ok = issue_qk(0);
+      if (ok && g_eff >= 2) ok = issue_qk(1);
+      for (int i = 0; i < total && ok; ++i) {
+        const int kt = i / g_eff, s = i % g_eff, st = i % C::NS, w = s & 1;
+        ok = mbar_wait(&bar_p_ready[w], wg_iter[w] & 1, abort_p);
+        if (!ok) break;
+        ++wg_iter[w];
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + C::TMEM_O + s * D, tmem + 128 * w + kk * 8,
+                  umma_desc(sv + st * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_o,
+                  (kt > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bar_kv_empty[st]);
+        umma_commit(&bar_o_done[s]);
+        // next iteration of the same warpgroup
+        int nxt = -1;
+        for (int j = i + 1; j < total; ++j)
+          if (((j % g_eff) & 1) == w) { nxt = j; break; }
+        if (nxt >= 0) ok = issue_qk(nxt);
+      }
+      // every issued MMA completes before TMEM can be released
+      umma_commit(&bar_drain);
+      volatile int no_abort = 0;
+      mbar_wait(&bar_drain, 0, &no_abort);
+    }
+    __syncwarp();
+  } else {
+    // =================== softmax warpgroups ================================
+    const int wg = (warp - 2) >> 2;                  // 0 or 1
+    const int quad = warp & 3;                       // TMEM lane quadrant
+    const int row = quad * 32 + lane;                // query row within the tile
+    const int j = jt * C::BM + row;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    const float c1 = kLog2e * rsqrtf((float)D);      // logit scale in log2 units
+    float m_run[C::G / 2], l_run[C::G / 2];
+#pragma unroll
+    for (int u = 0; u < C::G / 2; ++u) { m_run[u] = -INFINITY; l_run[u] = 0.f; }
+    bool ok = wg < n_wg;
+    int it = 0;  // iterations done by this warpgroup
+    for (int kt = 0; kt < nkt && ok; ++kt) {
+      const int bs = kt & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_bias_full[bs], (kt >> 1) & 1, abort_p));
+      if (!ok) break;
+      const uint8_t* btile = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
+#pragma unroll
+      for (int u = 0; u < C::G / 2; ++u) {
+        const int s = 2 * u + wg;
+        if (s >= g_eff) break;
+        const int i = kt * g_eff + s;
+        const int st = i % C::NS;
+        ok = mbar_wait(&bar_kv_full[st], (i / C::NS) & 1, abort_p) &&
+             mbar_wait(&bar_s_full[wg], it & 1, abort_p);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t x[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(lane_base + 128 * wg + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+        tmem_wait_ld();
+        const float* madd = reinterpret_cast<const float*>(smem + C::OFF_MADD + st * C::BN * 4);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float bv[8];
+          if (BIAS_K_CONTIG) {
+            const uint8_t* src = btile + (c >> 3) * (C::BIAS_TILE / 2) + row * 128 +
+                                 ((((c & 7) ^ (row & 7))) << 4);
+            const uint4 w4 = *reinterpret_cast<const uint4*>(src);
+            bv[0] = bf16lo(w4.x); bv[1] = bf16hi(w4.x); bv[2] = bf16lo(w4.y); bv[3] = bf16hi(w4.y);
+            bv[4] = bf16lo(w4.z); bv[5] = bf16hi(w4.z); bv[6] = bf16lo(w4.w); bv[7] = bf16hi(w4.w);
+          } else {
+            const int jj = row & 63;
+            const uint8_t* col = btile + (row >> 6) * (C::BIAS_TILE / 2) + (jj & 7) * 2;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int kk = c * 8 + e;
+              const uint16_t u16 = *reinterpret_cast<const uint16_t*>(
+                  col + kk * 128 + ((((jj >> 3) ^ (kk & 7))) << 4));
+              bv[e] = __uint_as_float((uint32_t)u16 << 16);
+            }
+          }
+          const float4 ma = *reinterpret_cast<const float4*>(madd + 8 * c);
+          const float4 mb = *reinterpret_cast<const float4*>(madd + 8 * c + 4);
+          const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float t = fmaf(__uint_as_float(x[8 * c + e]), c1, mv[e]);
+            t = fmaf(bv[e], kLog2e, t);
+            x[8 * c + e] = __float_as_uint(t);
+            mx = fmaxf(mx, t);
+          }
+        }
+        const float m_new = fmaxf(m_run[u], mx);
+        const float alpha = ex2(m_run[u] - m_new);
+        float sum = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const float p0 = ex2(__uint_as_float(x[2 * e]) - m_new);
+          const float p1 = ex2(__uint_as_float(x[2 * e + 1]) - m_new);
+          sum += p0 + p1;
+          pk[e] = pack_bf16(p0, p1);
+        }
+        l_run[u] = l_run[u] * alpha + sum;
+        m_run[u] = m_new;
+        // rescale O of this row when its running max moved (warp-uniform)
+        if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_done[s], (kt - 1) & 1, abort_p));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld16(lane_base + C::TMEM_O + s * D + 16 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(lane_base + C::TMEM_O + s * D + 16 * c, o);
+          }
+        }
+        tmem_st32(lane_base + 128 * wg, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(lane_base + 128 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_p_ready[wg]);
+        ++it;
+      }
+      if (!ok) break;
+      mbar_arrive(&bar_bias_empty[bs]);
+    }
+    // ---- epilogue: O / l, sigmoid gate, lse -------------------------------
+    if (ok) {
+#pragma unroll
+      for (int u = 0; u < C::G / 2; ++u) {
+        const int s = 2 * u + wg;
+        if (s >= g_eff) break;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_done[s], (nkt - 1) & 1, abort_p));
+        if (!ok) break;
+        tc_fence_after();
+        float o[D];
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t r[16];
+          tmem_ld16(lane_base + C::TMEM_O + s * D + 16 * c, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[16 * c + e] = __uint_as_float(r[e]);
+        }
+        if (j < p.N) {
+          const float inv_l = 1.0f / l_run[u];
+          const int ss = s0 + s;
+          const int64_t row_id = (((int64_t)b * p.S + ss) * p.H + h) * p.N + j;
+          p.lse[row_id] = (m_run[u] + __log2f(l_run[u])) * kLn2;
+          __nv_bfloat16* dst = p.out + p.o.at(b, ss, h, j, 0);
+          const __nv_bfloat16* gsrc = HAS_GATE ? p.gate + p.g.at(b, ss, h, j, 0) : nullptr;
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            float gv[8];
+            if (HAS_GATE) {
+              const uint4 g4 = *reinterpret_cast<const uint4*>(gsrc + 8 * c);
+              gv[0] = bf16lo(g4.x); gv[1] = bf16hi(g4.x); gv[2] = bf16lo(g4.y); gv[3] = bf16hi(g4.y);
+              gv[4] = bf16lo(g4.z); gv[5] = bf16hi(g4.z); gv[6] = bf16lo(g4.w); gv[7] = bf16hi(g4.w);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) gv[e] = 1.0f / (1.0f + ex2(-gv[e] * kLog2e));
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) gv[e] = 1.0f;
+            }
+            uint4 w4;
+            w4.x = pack_bf16(o[8 * c + 0] * inv_l * gv[0], o[8 * c + 1] * inv_l * gv[1]);
+            w4.y = pack_bf16(o[8 * c + 2] * inv_l * gv[2], o[8 * c + 3] * inv_l * gv[3]);
+            w4.z = pack_bf16(o[8 * c + 4] * inv_l * gv[4], o[8 * c + 5] * inv_l * gv[5]);
+            w4.w = pack_bf16(o[8 * c + 6] * inv_l * gv[6], o[8 * c + 7] * inv_l * gv[7]);
+            *reinterpret_cast<uint4*>(dst + 8 * c) = w4;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0) report_abort(abort_p, p.status);
+}
+
+// 5-D tensor map of a [B,S,H,N,D] bf16 view, box = 128 rows x D.
+bool tmap_rows(CUtensorMap* m, const void* base, const Strides5& st, const Problem& P) {
+  const uint64_t dims[5] = {(uint64_t)P.D, (uint64_t)P.N, (uint64_t)P.H, (uint64_t)P.S,
+                            (uint64_t)P.B};
+  const uint64_t str[4] = {(uint64_t)st.n * 2, (uint64_t)st.h * 2, (uint64_t)st.s * 2,
+                           (uint64_t)st.b * 2};
+  const uint32_t box[5] = {(uint32_t)P.D, 128, 1, 1, 1};
+  const CUtensorMapSwizzle sw = P.D == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                : P.D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                            : CU_TENSOR_MAP_SWIZZLE_128B;
+  return make_tmap_bf16(m, base, 5, dims, str, box, sw);
+}
+
+// 4-D tensor map of the pair bias with its contiguous axis innermost; box =
+// 64 (contiguous axis) x 128, 128-byte swizzle.
+bool tmap_bias(CUtensorMap* m, const void* base, const StridesBias& sb, const Problem& P,
+               bool k_contig) {
+  const uint64_t dims[4] = {(uint64_t)P.N, (uint64_t)P.N, (uint64_t)P.H, (uint64_t)P.B};
+  const uint64_t outer = k_contig ? sb.j : sb.k;
+  const uint64_t str[3] = {outer * 2, (uint64_t)sb.h * 2, (uint64_t)sb.b * 2};
+  const uint32_t box[4] = {64, 128, 1, 1};
+  return make_tmap_bf16(m, base, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int D, bool KC, bool GATE>
+cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& bias, const FwdParams& fp, unsigned grid,
+                       cudaStream_t st) {
+  using C = FwdCfg<D>;
+  auto kern = evoattn_fwd_kernel<D, KC, GATE>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(q, k, v, bias, fp);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t fwd_d(const Problem& P, const Bf16Ptrs& a, unsigned int* status, cudaStream_t st,
+                  bool* tmap_ok) {
+  using C = FwdCfg<D>;
+  CUtensorMap tq, tk, tv, tb;
+  const bool kc = P.bias.k == 1;
+  if (!tmap_rows(&tq, a.q, P.q, P) || !tmap_rows(&tk, a.k, P.k, P) ||
+      !tmap_rows(&tv, a.v, P.v, P) || !tmap_bias(&tb, a.bias, P.bias, P, kc)) {
+    *tmap_ok = false;
+    return cudaErrorInvalidValue;
+  }
+  FwdParams fp{};
+  fp.B = P.B; fp.S = P.S; fp.H = P.H; fp.N = P.N;
+  fp.n_jt = (P.N + C::BM - 1) / C::BM;
+  fp.n_kt = (P.N + C::BN - 1) / C::BN;
+  fp.n_sg = (P.S + C::G - 1) / C::G;
+  fp.mask = a.mask;
+  fp.msb = P.mask.b; fp.mss = P.mask.s; fp.msk = P.mask.k;
+  fp.gate = static_cast<const __nv_bfloat16*>(a.gate);
+  fp.g = P.g;
+  fp.out = static_cast<__nv_bfloat16*>(a.out);
+  fp.o = P.o;
+  fp.lse = a.lse;
+  fp.status = status;
+  const uint64_t grid64 = (uint64_t)fp.n_jt * P.H * fp.n_sg * P.B;
+  if (grid64 > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
+  const unsigned grid = (unsigned)grid64;
+  const bool gate = a.gate != nullptr;
+  if (kc) return gate ? launch_fwd<D, true, true>(tq, tk, tv, tb, fp, grid, st)
+                      : launch_fwd<D, true, false>(tq, tk, tv, tb, fp, grid, st);
+  return gate ? launch_fwd<D, false, true>(tq, tk, tv, tb, fp, grid, st)
+              : launch_fwd<D, false, false>(tq, tk, tv, tb, fp, grid, st);
+}
+
+}  // namespace
+
+cudaError_t bf16_fwd(const Problem& P, const Bf16Ptrs& a, unsigned int* status,
+                     cudaStream_t st, bool* tmap_ok) {
+  switch (P.D) {
+    case 16: return fwd_d<16>(P, a, status, st, tmap_ok);
+    case 32: return fwd_d<32>(P, a, status, st, tmap_ok);
+    case 64: return fwd_d<64>(P, a, status, st, tmap_ok);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace evo

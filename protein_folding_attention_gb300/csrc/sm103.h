@@ -1,0 +1,30 @@
+// Launchers of the tcgen05/TMA (sm_103a) kernels of the BF16 path.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "layout.cuh"
+
+namespace evo {
+
+struct Bf16Ptrs {
+  const void *q, *k, *v, *bias, *gate, *dout;
+  const unsigned char* mask;
+  void* out;   // forward: written; backward: read
+  float* lse;  // forward: written; backward: read
+  void *dq, *dk, *dv, *dgate;
+  float* dbias;
+};
+
+// Returns cudaSuccess or the first launch / tensor-map error.  `status` is the
+// device status word.  `tmap_ok` is set false when the driver rejected a
+// tensor map (alignment or size).
+cudaError_t bf16_fwd(const Problem& P, const Bf16Ptrs& a, unsigned int* status,
+                     cudaStream_t st, bool* tmap_ok);
+
+size_t bf16_bwd_workspace_bytes(const Problem& P, unsigned flags);
+cudaError_t bf16_bwd(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
+                     unsigned int* status, cudaStream_t st, bool* tmap_ok);
+
+}  // namespace evo

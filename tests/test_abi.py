@@ -1,0 +1,133 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/evoattn.h declares, and rejects bad arguments on the host with the
+documented status before touching the device (fake pointers are never
+dereferenced because validation fails first)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from protein_folding_attention_gb300 import build_lib, evoattn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return evoattn.load()
+
+
+def declared_entry_points():
+    text = open(os.path.join(ROOT, "include", "evoattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(evoattn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_entry_points()
+    assert {"evoattn_fwd", "evoattn_bwd", "evoattn_bwd_workspace_size",
+            "evoattn_get_device_status", "evoattn_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/evoattn.h but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = evoattn.status_string(code)
+        assert s and s != "unknown status"
+    assert evoattn.status_string(99) == "unknown status"
+    assert lib.evoattn_version() >= 100
+
+
+S5 = ctypes.c_int64 * 5
+S4 = ctypes.c_int64 * 4
+S3 = ctypes.c_int64 * 3
+FAKE = ctypes.c_void_p(1 << 20)  # 16-byte aligned, never dereferenced
+
+
+def dense5(B, S, H, N, D):
+    return S5(S * H * N * D, H * N * D, N * D, D, 1)
+
+
+def call_fwd(lib, *, q=FAKE, qs=None, bias=FAKE, bs=None, mask=None, ms=None, gate=None,
+             gs=None, out=FAKE, lse=FAKE, shape=(1, 4, 2, 64, 32), dtype=evoattn.BF16):
+    B, S, H, N, D = shape
+    qs = qs or dense5(*shape)
+    bs = bs or S4(H * N * N, N * N, N, 1)
+    return lib.evoattn_fwd(q, qs, FAKE, qs, FAKE, qs, bias, bs, mask, ms, gate, gs or qs,
+                           out, qs, lse, B, S, H, N, D, dtype, None)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    assert call_fwd(lib, q=None) == evoattn.ERR_INVALID_ARG
+    assert call_fwd(lib, bias=None) == evoattn.ERR_INVALID_ARG
+    assert call_fwd(lib, lse=None) == evoattn.ERR_INVALID_ARG
+    assert call_fwd(lib, shape=(1, 0, 2, 64, 32)) == evoattn.ERR_INVALID_ARG
+    assert call_fwd(lib, mask=FAKE, ms=None) == evoattn.ERR_INVALID_ARG
+    assert call_fwd(lib, shape=(1, 4, 2, 64, 48)) == evoattn.ERR_UNSUPPORTED
+    assert call_fwd(lib, shape=(1, 4, 2, 64, 128)) == evoattn.ERR_UNSUPPORTED  # bf16 D<=64
+    assert call_fwd(lib, dtype=7) == evoattn.ERR_UNSUPPORTED
+    neg = S5(-1, 1, 1, 1, 1)
+    assert call_fwd(lib, qs=neg) == evoattn.ERR_INVALID_ARG
+
+
+def test_fwd_bf16_alignment_rules(lib):
+    shape = (1, 4, 2, 64, 32)
+    # d stride must be 1
+    assert call_fwd(lib, qs=S5(2 * 4 * 2 * 64 * 32, 2 * 2 * 64 * 32, 2 * 64 * 32, 64, 2)) == \
+        evoattn.ERR_ALIGNMENT
+    # other strides multiples of 8 elements
+    assert call_fwd(lib, qs=S5(4 * 2 * 64 * 36, 2 * 64 * 36, 64 * 36, 36, 1)) == \
+        evoattn.ERR_ALIGNMENT
+    # 16-byte aligned base
+    assert call_fwd(lib, q=ctypes.c_void_p((1 << 20) + 8)) == evoattn.ERR_ALIGNMENT
+    # bias: unit stride along k or j, not neither
+    assert call_fwd(lib, bs=S4(2 * 64 * 64 * 8, 64 * 64 * 8, 64 * 8, 8)) == evoattn.ERR_ALIGNMENT
+    # bias row stride not a multiple of 8
+    assert call_fwd(lib, bs=S4(2 * 64 * 68, 64 * 68, 66, 1)) == evoattn.ERR_ALIGNMENT
+    # lse must be 16-byte aligned
+    assert call_fwd(lib, lse=ctypes.c_void_p((1 << 20) + 4)) == evoattn.ERR_ALIGNMENT
+    del shape
+
+
+def call_bwd(lib, *, gate=None, dgate=None, ws=FAKE, ws_bytes=1 << 40, flags=0,
+             shape=(1, 4, 2, 64, 32), dtype=evoattn.BF16, dq=FAKE):
+    B, S, H, N, D = shape
+    s = dense5(*shape)
+    bs = S4(H * N * N, N * N, N, 1)
+    return lib.evoattn_bwd(FAKE, s, FAKE, s, FAKE, s, FAKE, bs, None, None, gate, s, FAKE, s,
+                           FAKE, FAKE, s, dq, s, FAKE, s, FAKE, s, FAKE, dgate, s,
+                           B, S, H, N, D, dtype, flags, ws, ws_bytes, None)
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    assert call_bwd(lib, dq=None) == evoattn.ERR_INVALID_ARG
+    assert call_bwd(lib, gate=FAKE, dgate=None) == evoattn.ERR_INVALID_ARG
+    assert call_bwd(lib, gate=None, dgate=FAKE) == evoattn.ERR_INVALID_ARG
+    assert call_bwd(lib, flags=2) == evoattn.ERR_INVALID_ARG
+    assert call_bwd(lib, ws=None) == evoattn.ERR_WORKSPACE
+    assert call_bwd(lib, ws_bytes=16) == evoattn.ERR_WORKSPACE
+    assert call_bwd(lib, ws=ctypes.c_void_p((1 << 20) + 16)) == evoattn.ERR_WORKSPACE
+    assert call_bwd(lib, shape=(1, 4, 2, 64, 24)) == evoattn.ERR_UNSUPPORTED
+
+
+def test_workspace_is_linear_not_cubic(lib):
+    for dt in (torch_bf16(), torch_f32()):
+        small = evoattn.workspace_size(1, 64, 4, 256, 32, dt)
+        assert small > 0
+        big = evoattn.workspace_size(1, 768, 4, 768, 32, dt)
+        cubic = 1 * 768 * 4 * 768 * 768 * 2  # bf16 logits of the whole problem
+        assert big < cubic / 4
+    assert evoattn.workspace_size(1, 8, 2, 64, 48) == 0
+
+
+def torch_bf16():
+    import torch
+    return torch.bfloat16
+
+
+def torch_f32():
+    import torch
+    return torch.float32
