@@ -1,14 +1,942 @@
-// EvoAttention backward on sm_103a (placeholder until the kernels land).
+// EvoAttention backward on sm_103a.
+//
+// MegaFold technical summary, "Methodik" section 1 "EvoFlash-3D": the
+// backward pass recomputes the logits tile by tile in on-chip memory, as the
+// forward does, so the B*S*H*N*N attention map never reaches HBM; its
+// pair-bias term receives the gradient summed over the S rows that share it.
+//
+// With P = exp(x - lse), dOa = dout * sigmoid(g) and delta = rowsum(dOa * O):
+//   dP = dOa V^T,  dS = P * (dP - delta),
+//   dV = P^T dOa,  dK = dS^T Q / sqrt(D),  dQ = dS K / sqrt(D),
+//   dbias[b,h,j,k] = sum_s dS[b,s,h,j,k],  dgate = dout * out * (1 - sigmoid(g)).
+// The three reductions run along three different axes (dK, dV over query
+// tiles, dQ over key tiles, dbias over s), so they are split over kernels:
+//
+//   k_pre    delta, dgate and dOa (bf16) per row; zeroes the fp32 dQ buffer
+//   k_dkdv   CTA = (b, s, h, key tile): loops over query tiles with dK, dV
+//            accumulating in tensor memory; dQ partial sums are added into
+//            the fp32 buffer with vector atomics
+//   k_dbias  CTA = (b, h, query tile, key tile, s-slot): loops over the s of
+//            its slot, recomputing S and dP, accumulating dS in tensor memory;
+//            writes one partial per slot (or adds it atomically)
+//   k_reduce ordered sum of the slot partials -> dbias; fp32 dQ -> bf16 dq
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "layout.cuh"
 #include "sm103.h"
+#include "tmap.h"
 
 namespace evo {
+namespace {
 
-size_t bf16_bwd_workspace_bytes(const Problem& P, unsigned) {
-  return (size_t)P.rows() * 4 + 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
 }
 
-cudaError_t bf16_bwd(const Problem&, const Bf16Ptrs&, unsigned, void*, unsigned int*,
-                     cudaStream_t, bool*) {
+// ---------------------------------------------------------------------------
+// Workspace layout
+// ---------------------------------------------------------------------------
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Number of s-slots of the dbias reduction: enough CTAs for a few waves on a
+// 152-SM part, fixed by the problem shape alone (so the summation order, and
+// hence every bit of dbias, does not depend on the device).
+inline int dbias_slots(const Problem& P) {
+  const int nt = (P.N + 127) / 128;
+  const long tiles = (long)P.B * P.H * nt * nt;
+  long slots = (4L * 152 + tiles - 1) / tiles;
+  if (slots < 1) slots = 1;
+  if (slots > P.S) slots = P.S;
+  return (int)slots;
+}
+
+struct Workspace {
+  __nv_bfloat16* dOa;  // [B,S,H,N,D] dense
+  float* delta;        // [B,S,H,N]
+  float* dq_acc;       // [B,S,H,N,D] dense fp32
+  float* partial;      // [slots, B, H, N, N] fp32 (deterministic mode)
+  size_t bytes;
+};
+
+Workspace carve(const Problem& P, unsigned flags, void* base) {
+  const size_t L = (size_t)P.rows() * P.D;
+  size_t off = 0;
+  Workspace w{};
+  uint8_t* b = static_cast<uint8_t*>(base);
+  w.dOa = reinterpret_cast<__nv_bfloat16*>(b + off); off = align256(off + L * 2);
+  w.delta = reinterpret_cast<float*>(b + off); off = align256(off + (size_t)P.rows() * 4);
+  w.dq_acc = reinterpret_cast<float*>(b + off); off = align256(off + L * 4);
+  w.partial = reinterpret_cast<float*>(b + off);
+  if (!(flags & EVOATTN_DBIAS_ATOMIC))
+    off = align256(off + (size_t)dbias_slots(P) * P.B * P.H * P.N * P.N * 4);
+  w.bytes = off;
+  return w;
+}
+
+// ---------------------------------------------------------------------------
+// k_pre: per row, D/8 threads of 8 features each.
+// ---------------------------------------------------------------------------
+struct PreParams {
+  int B, S, H, N, D;
+  const __nv_bfloat16 *out, *dout, *gate;
+  Strides5 o, dO, g, dg;
+  __nv_bfloat16* dgate;
+  __nv_bfloat16* dOa;
+  float* delta;
+  float* dq_acc;
+};
+
+__device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
+  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+  f[4] = bf16lo(u.z); f[5] = bf16hi(u.z); f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                    pack_bf16(f[6], f[7]));
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) k_pre(const PreParams p) {
+  constexpr int TPR = D / 8;  // threads per row
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t rows = (int64_t)p.B * p.S * p.H * p.N;
+  const int64_t row = t / TPR;
+  const int part = (int)(t % TPR);
+  const bool live = row < rows;
+  float dl = 0.f;
+  if (live) {
+    const int j = (int)(row % p.N);
+    const int h = (int)((row / p.N) % p.H);
+    const int s = (int)((row / ((int64_t)p.N * p.H)) % p.S);
+    const int b = (int)(row / ((int64_t)p.N * p.H * p.S));
+    float o[8], go[8], sg[8];
+    unpack8(*reinterpret_cast<const uint4*>(p.out + p.o.at(b, s, h, j, 8 * part)), o);
+    unpack8(*reinterpret_cast<const uint4*>(p.dout + p.dO.at(b, s, h, j, 8 * part)), go);
+    if (p.gate) {
+      float g[8], dg[8];
+      unpack8(*reinterpret_cast<const uint4*>(p.gate + p.g.at(b, s, h, j, 8 * part)), g);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sg[e] = 1.0f / (1.0f + ex2(-g[e] * kLog2e));
+        dg[e] = go[e] * o[e] * (1.0f - sg[e]);
+      }
+      *reinterpret_cast<uint4*>(p.dgate + p.dg.at(b, s, h, j, 8 * part)) = pack8(dg);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sg[e] = 1.0f;
+    }
+    float a[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      dl = fmaf(go[e], o[e], dl);
+      a[e] = go[e] * sg[e];
+    }
+    *reinterpret_cast<uint4*>(p.dOa + row * D + 8 * part) = pack8(a);
+    float4* z = reinterpret_cast<float4*>(p.dq_acc + row * D + 8 * part);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, off);
+  if (live && part == 0) p.delta[row] = dl;
+}
+
+// ---------------------------------------------------------------------------
+// Shared tile configuration of the tcgen05 kernels
+// ---------------------------------------------------------------------------
+template <int D>
+struct Tile {
+  static constexpr uint32_t ROW = D * 2;
+  static constexpr uint32_t ATOM = 8 * ROW;
+  static constexpr Swizzle SW = D == 16 ? kSw32 : kSw64;
+  static constexpr uint32_t TILE = 128 * ROW;
+  static constexpr uint32_t BIAS_TILE = 128 * 128 * 2;
+};
+
+// bias[j, k] of a 128x128 tile staged by TMA as two 64-wide boxes with a
+// 128-byte swizzle.  K_CONTIG: rows are j (keys contiguous), otherwise rows
+// are k (queries contiguous).
+template <bool K_CONTIG>
+__device__ __forceinline__ float bias_at(const uint8_t* tile, int j, int k) {
+  const int r = K_CONTIG ? j : k;   // smem row
+  const int c = K_CONTIG ? k : j;   // contiguous index
+  const uint8_t* p = tile + (c >> 6) * 16384 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) +
+                     (c & 7) * 2;
+  return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(p)) << 16);
+}
+
+// ---------------------------------------------------------------------------
+// k_dkdv
+// ---------------------------------------------------------------------------
+// Warps: 0 TMA producer, 1 MMA issuer, 2-9 two compute warpgroups.  A compute
+// thread owns key k (TMEM lane 32*(warp%4)+lane) and, of each 128-query tile,
+// the 64 queries of its warpgroup's half.  Tensor memory columns:
+//   S^T 0..127, dP^T 128..255 (fp32, lane = key), P^T 256.., dS^T 320..
+//   (bf16 pairs, 32 columns per warpgroup half), dQ partial 384.. (lane =
+//   query), dK 384+D.., dV 384+2D.. (lane = key).
+template <int D>
+struct DkdvCfg : Tile<D> {
+  using T = Tile<D>;
+  static constexpr int NQ = 2;  // query-tile pipeline stages
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + T::TILE;
+  static constexpr uint32_t OFF_Q = OFF_V + T::TILE;
+  static constexpr uint32_t OFF_DO = OFF_Q + NQ * T::TILE;
+  static constexpr uint32_t OFF_BIAS = OFF_DO + NQ * T::TILE;
+  static constexpr uint32_t OFF_DS = OFF_BIAS + NQ * T::BIAS_TILE;
+  static constexpr uint32_t OFF_LD = OFF_DS + 128 * 128 * 2;  // lse2[128], delta[128] per stage
+  static constexpr uint32_t SMEM = OFF_LD + NQ * 256 * 4;
+  static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_P = 256, T_DS = 320, T_DQ = 384,
+                            T_DK = 384 + D, T_DV = 384 + 2 * D;
+};
+
+struct DkdvParams {
+  int B, S, H, N, njt, nkt;
+  const unsigned char* mask;
+  int64_t msb, mss, msk;
+  const float* lse;
+  const float* delta;
+  float* dq_acc;
+  __nv_bfloat16 *dk, *dv;
+  Strides5 sdk, sdv;
+  unsigned int* status;
+};
+
+template <int D, bool BIAS_K_CONTIG>
+__global__ void __launch_bounds__(320, 1)
+    k_dkdv(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+           const __grid_constant__ CUtensorMap tm_bias, const DkdvParams p) {
+  using C = DkdvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bar_kv, bar_qd_full[C::NQ], bar_qd_empty[C::NQ], bar_b_full[C::NQ],
+      bar_b_empty[C::NQ], bar_s_full, bar_sdp_free, bar_p_ready, bar_mma_done, bar_dq_free,
+      bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  int idx = blockIdx.x;
+  const int kt = idx % p.nkt; idx /= p.nkt;
+  const int h = idx % p.H; idx /= p.H;
+  const int s = idx % p.S;
+  const int b = idx / p.S;
+  const int njt = p.njt;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_kv, 1);
+    for (int i = 0; i < C::NQ; ++i) {
+      mbar_init(&bar_qd_full[i], 1); mbar_init(&bar_qd_empty[i], 1);
+      mbar_init(&bar_b_full[i], 1); mbar_init(&bar_b_empty[i], 256);
+    }
+    mbar_init(&bar_s_full, 1); mbar_init(&bar_sdp_free, 256); mbar_init(&bar_p_ready, 256);
+    mbar_init(&bar_mma_done, 1); mbar_init(&bar_dq_free, 256); mbar_init(&bar_drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_slot, 512);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do); tma_prefetch_desc(&tm_bias);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort_p = &abort_flag;
+  const int64_t row0 = (((int64_t)b * p.S + s) * p.H + h) * p.N;  // row of (b,s,h,0)
+
+  if (warp == 0) {
+    // ============================ producer =================================
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar_kv, 2 * C::TILE);
+      tma_load_5d(smem + C::OFF_K, &tm_k, &bar_kv, 0, kt * 128, h, s, b);
+      tma_load_5d(smem + C::OFF_V, &tm_v, &bar_kv, 0, kt * 128, h, s, b);
+    }
+    bool ok = true;
+    int issued = 0;
+    for (int jt = 0; jt < njt; ++jt) {
+      const int st = jt % C::NQ;
+      if (jt >= C::NQ) {
+        ok = mbar_wait(&bar_qd_empty[st], ((jt / C::NQ) - 1) & 1, abort_p) &&
+             mbar_wait(&bar_b_empty[st], ((jt / C::NQ) - 1) & 1, abort_p);
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      // per-query constants of this tile: lse in log2 units (+inf beyond N so
+      // that P = 0 there) and delta
+      float* ld = reinterpret_cast<float*>(smem + C::OFF_LD + st * 1024);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int jl = e * 32 + lane, j = jt * 128 + jl;
+        ld[jl] = j < p.N ? p.lse[row0 + j] * kLog2e : INFINITY;
+        ld[128 + jl] = j < p.N ? p.delta[row0 + j] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar_qd_full[st], 2 * C::TILE);
+        tma_load_5d(smem + C::OFF_Q + st * C::TILE, &tm_q, &bar_qd_full[st], 0, jt * 128, h, s, b);
+        tma_load_5d(smem + C::OFF_DO + st * C::TILE, &tm_do, &bar_qd_full[st], 0, jt * 128, h, s,
+                    b);
+        uint8_t* dst = smem + C::OFF_BIAS + st * C::BIAS_TILE;
+        mbar_arrive_expect_tx(&bar_b_full[st], C::BIAS_TILE);
+        if (BIAS_K_CONTIG) {
+          tma_load_4d(dst, &tm_bias, &bar_b_full[st], kt * 128, jt * 128, h, b);
+          tma_load_4d(dst + 16384, &tm_bias, &bar_b_full[st], kt * 128 + 64, jt * 128, h, b);
+        } else {
+          tma_load_4d(dst, &tm_bias, &bar_b_full[st], jt * 128, kt * 128, h, b);
+          tma_load_4d(dst + 16384, &tm_bias, &bar_b_full[st], jt * 128 + 64, kt * 128, h, b);
+        }
+      }
+      issued = jt + 1;
+    }
+    if (!ok && lane == 0) {
+      volatile int no_abort = 0;
+      for (int jt = max(0, issued - C::NQ); jt < issued; ++jt) {
+        mbar_wait(&bar_qd_full[jt % C::NQ], (jt / C::NQ) & 1, &no_abort);
+        mbar_wait(&bar_b_full[jt % C::NQ], (jt / C::NQ) & 1, &no_abort);
+      }
+      mbar_wait(&bar_kv, 0, &no_abort);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ============================ MMA issuer ===============================
+    if (lane == 0) {
+      constexpr uint32_t id_sdp = idesc_bf16(128, 128, 0, 0);  // A=K/V, B=Q/dOa, K-major
+      constexpr uint32_t id_kv = idesc_bf16(128, D, 0, 1);     // A=P^T/dS^T (TMEM), B MN-major
+      constexpr uint32_t id_q = idesc_bf16(128, D, 1, 1);      // A=dS (smem, MN-major)
+      const uint32_t sk = smem_u32(smem + C::OFF_K), sv = smem_u32(smem + C::OFF_V),
+                     sq = smem_u32(smem + C::OFF_Q), sdo = smem_u32(smem + C::OFF_DO),
+                     sds = smem_u32(smem + C::OFF_DS);
+      bool ok = mbar_wait(&bar_kv, 0, abort_p);
+      auto issue_sdp = [&](int jt) -> bool {
+        const int st = jt % C::NQ;
+        if (!mbar_wait(&bar_qd_full[st], (jt / C::NQ) & 1, abort_p)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          umma_ss(tmem + C::T_S, umma_desc(sk + kk * 32, 16, C::ATOM, C::SW),
+                  umma_desc(sq + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_sdp, kk > 0);
+          umma_ss(tmem + C::T_DP, umma_desc(sv + kk * 32, 16, C::ATOM, C::SW),
+                  umma_desc(sdo + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_sdp, kk > 0);
+        }
+        umma_commit(&bar_s_full);
+        return true;
+      };
+      if (ok) ok = issue_sdp(0);
+      for (int jt = 0; jt < njt && ok; ++jt) {
+        const int st = jt % C::NQ;
+        // S/dP of jt are in registers: the next tile may overwrite them
+        if (jt + 1 < njt) {
+          ok = mbar_wait(&bar_sdp_free, jt & 1, abort_p);
+          if (ok) ok = issue_sdp(jt + 1);
+          if (!ok) break;
+        }
+        ok = mbar_wait(&bar_p_ready, jt & 1, abort_p);
+        if (ok && jt > 0) ok = mbar_wait(&bar_dq_free, (jt - 1) & 1, abort_p);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t acc = (jt > 0 || kk > 0) ? 1u : 0u;
+          // dV += P^T dOa ; dK += dS^T Q  (K dimension = queries, 16 per step)
+          umma_ts(tmem + C::T_DV, tmem + C::T_P + kk * 8,
+                  umma_desc(sdo + st * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_kv,
+                  acc);
+          umma_ts(tmem + C::T_DK, tmem + C::T_DS + kk * 8,
+                  umma_desc(sq + st * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_kv,
+                  acc);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K dimension = keys)
+          umma_ss(tmem + C::T_DQ, umma_desc(sds + kk * 2048, 16384, 1024, kSw128),
+                  umma_desc(sk + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_q, kk > 0);
+        umma_commit(&bar_qd_empty[st]);
+        umma_commit(&bar_mma_done);
+      }
+      umma_commit(&bar_drain);
+      volatile int no_abort = 0;
+      mbar_wait(&bar_drain, 0, &no_abort);
+    }
+    __syncwarp();
+  } else {
+    // ============================ compute ==================================
+    const int wg = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int kl = quad * 32 + lane;          // key within the tile (TMEM lane)
+    const int kg = kt * 128 + kl;             // key index
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    const float c1 = kLog2e * rsqrtf((float)D);
+    const float inv_sqrt_d = rsqrtf((float)D);
+    // additive mask of this key, log2 units (constant over the query tiles)
+    float madd = 0.f;
+    if (kg >= p.N) madd = -INFINITY;
+    else if (p.mask && !p.mask[b * p.msb + (int64_t)s * p.mss + (int64_t)kg * p.msk])
+      madd = kMaskBias * kLog2e;
+    bool ok = true;
+    for (int jt = 0; jt < njt; ++jt) {
+      const int st = jt % C::NQ;
+      ok = mbar_wait(&bar_s_full, jt & 1, abort_p) &&
+           mbar_wait(&bar_qd_full[st], (jt / C::NQ) & 1, abort_p) &&
+           mbar_wait(&bar_b_full[st], (jt / C::NQ) & 1, abort_p);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sx[64], dpx[64];
+      tmem_ld32(lane_base + C::T_S + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&sx[0]));
+      tmem_ld32(lane_base + C::T_S + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&sx[32]));
+      tmem_ld32(lane_base + C::T_DP + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&dpx[0]));
+      tmem_ld32(lane_base + C::T_DP + 64 * wg + 32,
+                *reinterpret_cast<uint32_t(*)[32]>(&dpx[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bar_sdp_free);
+      const float* ld = reinterpret_cast<const float*>(smem + C::OFF_LD + st * 1024);
+      const uint8_t* btile = smem + C::OFF_BIAS + st * C::BIAS_TILE;
+      uint32_t pk[32], dk2[32];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {  // 4 queries per step
+        const float4 l4 = *reinterpret_cast<const float4*>(ld + 64 * wg + 4 * c);
+        const float4 d4 = *reinterpret_cast<const float4*>(ld + 128 + 64 * wg + 4 * c);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pv[4], dsv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int jl = 64 * wg + 4 * c + e;
+          const float bias = bias_at<BIAS_K_CONTIG>(btile, jl, kl);
+          float t = fmaf(__uint_as_float(sx[4 * c + e]), c1, madd);
+          t = fmaf(bias, kLog2e, t);
+          pv[e] = ex2(t - lv[e]);
+          dsv[e] = pv[e] * (__uint_as_float(dpx[4 * c + e]) - dv[e]) * inv_sqrt_d;
+        }
+        pk[2 * c] = pack_bf16(pv[0], pv[1]);
+        pk[2 * c + 1] = pack_bf16(pv[2], pv[3]);
+        dk2[2 * c] = pack_bf16(dsv[0], dsv[1]);
+        dk2[2 * c + 1] = pack_bf16(dsv[2], dsv[3]);
+      }
+      mbar_arrive(&bar_b_empty[st]);
+      // P^T and dS^T into tensor memory (A operands of dV, dK); the previous
+      // tile's MMAs are complete (waited in the dQ step below).
+      tmem_st32(lane_base + C::T_P + 32 * wg, pk);
+      tmem_st32(lane_base + C::T_DS + 32 * wg, dk2);
+      // dS into shared memory as the M-major A operand of dQ = dS K: row k,
+      // queries of this half contiguous, 128-byte swizzle.
+      {
+        uint8_t* rowp = smem + C::OFF_DS + wg * 16384 + (kl >> 3) * 1024 + (kl & 7) * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(rowp + ((c ^ (kl & 7)) << 4)) =
+              make_uint4(dk2[4 * c], dk2[4 * c + 1], dk2[4 * c + 2], dk2[4 * c + 3]);
+      }
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_p_ready);
+      // dQ partial of this (query tile, key tile): lane = query; this
+      // warpgroup adds its half of the D features.
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done, jt & 1, abort_p));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        uint32_t q16[D / 2];
+        if constexpr (D == 32) {
+          tmem_ld16(lane_base + C::T_DQ + 16 * wg, *reinterpret_cast<uint32_t(*)[16]>(&q16[0]));
+        } else {
+          uint32_t tmp[16];
+          tmem_ld16(lane_base + C::T_DQ, tmp);  // D = 16: both halves read, each adds 8
+#pragma unroll
+          for (int e = 0; e < 8; ++e) q16[e] = tmp[8 * wg + e];
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bar_dq_free);
+        const int jg = jt * 128 + kl;  // this lane's query row
+        if (jg < p.N) {
+          float* dst = p.dq_acc + (row0 + jg) * D + (D / 2) * wg;
+#pragma unroll
+          for (int e = 0; e < D / 2; e += 4)
+            red_add_v4(dst + e, __uint_as_float(q16[e]), __uint_as_float(q16[e + 1]),
+                       __uint_as_float(q16[e + 2]), __uint_as_float(q16[e + 3]));
+        }
+      }
+    }
+    // ---- dK (warpgroup 0) and dV (warpgroup 1) of this key tile -----------
+    if (ok) {
+      uint32_t r[D];
+      const uint32_t col = wg == 0 ? C::T_DK : C::T_DV;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c)
+        tmem_ld16(lane_base + col + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * c]));
+      tmem_wait_ld();
+      if (kg < p.N) {
+        __nv_bfloat16* dst =
+            wg == 0 ? p.dk + p.sdk.at(b, s, h, kg, 0) : p.dv + p.sdv.at(b, s, h, kg, 0);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * c + e]);
+          *reinterpret_cast<uint4*>(dst + 8 * c) = pack8(f);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0) report_abort(abort_p, p.status);
+}
+
+// ---------------------------------------------------------------------------
+// k_dbias
+// ---------------------------------------------------------------------------
+// CTA = (b, h, query tile jt, key tile kt, s-slot).  Warps: 0 producer, 1 MMA,
+// 2-9 two compute warpgroups; a compute thread owns query j (TMEM lane) and
+// the 64 keys of its warpgroup's half.  Tensor memory: S 0..127, dP
+// 128..255, dbias accumulator 256..383 (fp32, lane = query).
+template <int D>
+struct DbiasCfg : Tile<D> {
+  using T = Tile<D>;
+  static constexpr int NST = 2;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_DO = OFF_Q + NST * T::TILE;
+  static constexpr uint32_t OFF_K = OFF_DO + NST * T::TILE;
+  static constexpr uint32_t OFF_V = OFF_K + NST * T::TILE;
+  static constexpr uint32_t OFF_BIAS = OFF_V + NST * T::TILE;
+  static constexpr uint32_t OFF_MADD = OFF_BIAS + T::BIAS_TILE;
+  static constexpr uint32_t SMEM = OFF_MADD + NST * 128 * 4;
+  static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_ACC = 256;
+};
+
+struct DbiasParams {
+  int B, S, H, N, njt, nkt, slots;
+  const unsigned char* mask;
+  int64_t msb, mss, msk;
+  const float* lse;
+  const float* delta;
+  float* out;       // partial [slots,B,H,N,N] or dbias [B,H,N,N]
+  int atomic;
+  unsigned int* status;
+};
+
+template <int D, bool BIAS_K_CONTIG>
+__global__ void __launch_bounds__(320, 1)
+    k_dbias(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+            const __grid_constant__ CUtensorMap tm_bias, const DbiasParams p) {
+  using C = DbiasCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bar_bias, bar_full[C::NST], bar_empty[C::NST], bar_s_full, bar_sdp_free,
+      bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  int idx = blockIdx.x;
+  const int kt = idx % p.nkt; idx /= p.nkt;
+  const int jt = idx % p.njt; idx /= p.njt;
+  const int slot = idx % p.slots; idx /= p.slots;
+  const int h = idx % p.H;
+  const int b = idx / p.H;
+  // contiguous s range of this slot
+  const int s_begin = (int)(((int64_t)p.S * slot) / p.slots);
+  const int s_end = (int)(((int64_t)p.S * (slot + 1)) / p.slots);
+  const int ns = s_end - s_begin;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_bias, 1);
+    // a stage is empty once its MMAs completed (one commit) and both compute
+    // warpgroups are done with its key mask (256 arrivals)
+    for (int i = 0; i < C::NST; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_empty[i], 257); }
+    mbar_init(&bar_s_full, 1); mbar_init(&bar_sdp_free, 256); mbar_init(&bar_drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_slot, 512);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do); tma_prefetch_desc(&tm_bias);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort_p = &abort_flag;
+
+  if (warp == 0) {
+    // ============================ producer =================================
+    if (lane == 0) {
+      uint8_t* dst = smem + C::OFF_BIAS;
+      mbar_arrive_expect_tx(&bar_bias, C::BIAS_TILE);
+      if (BIAS_K_CONTIG) {
+        tma_load_4d(dst, &tm_bias, &bar_bias, kt * 128, jt * 128, h, b);
+        tma_load_4d(dst + 16384, &tm_bias, &bar_bias, kt * 128 + 64, jt * 128, h, b);
+      } else {
+        tma_load_4d(dst, &tm_bias, &bar_bias, jt * 128, kt * 128, h, b);
+        tma_load_4d(dst + 16384, &tm_bias, &bar_bias, jt * 128 + 64, kt * 128, h, b);
+      }
+    }
+    bool ok = true;
+    int issued = 0;
+    for (int i = 0; i < ns; ++i) {
+      const int st = i % C::NST, s = s_begin + i;
+      if (i >= C::NST) ok = mbar_wait(&bar_empty[st], ((i / C::NST) - 1) & 1, abort_p);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      float* madd = reinterpret_cast<float*>(smem + C::OFF_MADD + st * 512);
+      const unsigned char* mrow = p.mask ? p.mask + b * p.msb + (int64_t)s * p.mss : nullptr;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int kk = kt * 128 + e * 32 + lane;
+        float a = 0.f;
+        if (kk >= p.N) a = -INFINITY;
+        else if (mrow && !mrow[kk * p.msk]) a = kMaskBias * kLog2e;
+        madd[e * 32 + lane] = a;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar_full[st], 4 * C::TILE);
+        tma_load_5d(smem + C::OFF_Q + st * C::TILE, &tm_q, &bar_full[st], 0, jt * 128, h, s, b);
+        tma_load_5d(smem + C::OFF_DO + st * C::TILE, &tm_do, &bar_full[st], 0, jt * 128, h, s, b);
+        tma_load_5d(smem + C::OFF_K + st * C::TILE, &tm_k, &bar_full[st], 0, kt * 128, h, s, b);
+        tma_load_5d(smem + C::OFF_V + st * C::TILE, &tm_v, &bar_full[st], 0, kt * 128, h, s, b);
+      }
+      issued = i + 1;
+    }
+    if (!ok && lane == 0) {
+      volatile int no_abort = 0;
+      for (int i = max(0, issued - C::NST); i < issued; ++i)
+        mbar_wait(&bar_full[i % C::NST], (i / C::NST) & 1, &no_abort);
+      mbar_wait(&bar_bias, 0, &no_abort);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ============================ MMA issuer ===============================
+    if (lane == 0) {
+      constexpr uint32_t id = idesc_bf16(128, 128, 0, 0);
+      const uint32_t sq = smem_u32(smem + C::OFF_Q), sdo = smem_u32(smem + C::OFF_DO),
+                     sk = smem_u32(smem + C::OFF_K), sv = smem_u32(smem + C::OFF_V);
+      bool ok = true;
+      for (int i = 0; i < ns && ok; ++i) {
+        const int st = i % C::NST;
+        ok = mbar_wait(&bar_full[st], (i / C::NST) & 1, abort_p);
+        if (ok && i > 0) ok = mbar_wait(&bar_sdp_free, (i - 1) & 1, abort_p);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          umma_ss(tmem + C::T_S, umma_desc(sq + st * C::TILE + kk * 32, 16, C::ATOM, C::SW),
+                  umma_desc(sk + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id, kk > 0);
+          umma_ss(tmem + C::T_DP, umma_desc(sdo + st * C::TILE + kk * 32, 16, C::ATOM, C::SW),
+                  umma_desc(sv + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id, kk > 0);
+        }
+        umma_commit(&bar_empty[st]);
+        umma_commit(&bar_s_full);
+      }
+      umma_commit(&bar_drain);
+      volatile int no_abort = 0;
+      mbar_wait(&bar_drain, 0, &no_abort);
+    }
+    __syncwarp();
+  } else {
+    // ============================ compute ==================================
+    const int wg = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int jl = quad * 32 + lane;
+    const int jg = jt * 128 + jl;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    const float c1 = kLog2e * rsqrtf((float)D);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_bias, 0, abort_p));
+    const uint8_t* btile = smem + C::OFF_BIAS;
+    for (int i = 0; i < ns && ok; ++i) {
+      const int st = i % C::NST, s = s_begin + i;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, i & 1, abort_p));
+      if (!ok) break;
+      tc_fence_after();
+      const int64_t row = (((int64_t)b * p.S + s) * p.H + h) * p.N + jg;
+      const float lse2 = jg < p.N ? p.lse[row] * kLog2e : INFINITY;
+      const float dl = jg < p.N ? p.delta[row] : 0.f;
+      const float* madd = reinterpret_cast<const float*>(smem + C::OFF_MADD + st * 512);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sx[32], dpx[32], a[32];
+        const uint32_t col = C::T_ACC + 64 * wg + 32 * half;
+        tmem_ld32(lane_base + C::T_S + 64 * wg + 32 * half, sx);
+        tmem_ld32(lane_base + C::T_DP + 64 * wg + 32 * half, dpx);
+        if (i > 0) tmem_ld32(lane_base + col, a);
+        tmem_wait_ld();
+        if (half == 1) {  // S and dP of this s are in registers
+          tc_fence_before();
+          mbar_arrive(&bar_sdp_free);
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 8) {
+          const int k0 = 64 * wg + 32 * half + c;  // key within the tile
+          float bv[8];
+          if (BIAS_K_CONTIG) {
+            const uint4 w4 = *reinterpret_cast<const uint4*>(
+                btile + (k0 >> 6) * 16384 + jl * 128 + ((((k0 & 63) >> 3) ^ (jl & 7)) << 4));
+            unpack8(w4, bv);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bv[e] = bias_at<false>(btile, jl, k0 + e);
+          }
+          const float4 m4a = *reinterpret_cast<const float4*>(madd + k0);
+          const float4 m4b = *reinterpret_cast<const float4*>(madd + k0 + 4);
+          const float mv[8] = {m4a.x, m4a.y, m4a.z, m4a.w, m4b.x, m4b.y, m4b.z, m4b.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float t = fmaf(__uint_as_float(sx[c + e]), c1, mv[e]);
+            t = fmaf(bv[e], kLog2e, t);
+            const float pr = ex2(t - lse2);
+            const float ds = pr * (__uint_as_float(dpx[c + e]) - dl);
+            a[c + e] = __float_as_uint(i > 0 ? __uint_as_float(a[c + e]) + ds : ds);
+          }
+        }
+        tmem_st32(lane_base + col, a);
+      }
+      tmem_wait_st();
+      mbar_arrive(&bar_empty[st]);
+    }
+    // ---- write this slot's partial (or add it atomically) ------------------
+    if (ok && ns > 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t a[32];
+        tmem_ld32(lane_base + C::T_ACC + 64 * wg + 32 * half, a);
+        tmem_wait_ld();
+        const int k0 = kt * 128 + 64 * wg + 32 * half;
+        if (jg < p.N) {
+          const int64_t base = ((int64_t)b * p.H + h) * p.N * p.N + (int64_t)jg * p.N;
+          float* dst = p.atomic ? p.out + base
+                                : p.out + (int64_t)slot * p.B * p.H * p.N * p.N + base;
+          if (k0 + 32 <= p.N && (p.N & 3) == 0) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              if (p.atomic)
+                red_add_v4(dst + k0 + c, __uint_as_float(a[c]), __uint_as_float(a[c + 1]),
+                           __uint_as_float(a[c + 2]), __uint_as_float(a[c + 3]));
+              else
+                *reinterpret_cast<float4*>(dst + k0 + c) =
+                    make_float4(__uint_as_float(a[c]), __uint_as_float(a[c + 1]),
+                                __uint_as_float(a[c + 2]), __uint_as_float(a[c + 3]));
+            }
+          } else {
+            for (int c = 0; c < 32; ++c)
+              if (k0 + c < p.N) {
+                if (p.atomic) atomicAdd(dst + k0 + c, __uint_as_float(a[c]));
+                else dst[k0 + c] = __uint_as_float(a[c]);
+              }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0) report_abort(abort_p, p.status);
+}
+
+// ---------------------------------------------------------------------------
+// k_reduce: dbias = ordered sum of the slot partials; dq = bf16(dq_acc)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_dbias_sum(const float* __restrict__ partial,
+                                                   float* __restrict__ dbias, int64_t n,
+                                                   int slots) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if ((n & 3) == 0) {
+    const int64_t n4 = n >> 2;
+    if (i >= n4) return;
+    const float4* src = reinterpret_cast<const float4*>(partial);
+    float4 acc = src[i];
+    for (int sl = 1; sl < slots; ++sl) {
+      const float4 v = src[(int64_t)sl * n4 + i];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    reinterpret_cast<float4*>(dbias)[i] = acc;
+  } else {
+    if (i >= n) return;
+    float acc = partial[i];
+    for (int sl = 1; sl < slots; ++sl) acc += partial[(int64_t)sl * n + i];
+    dbias[i] = acc;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) k_dq_convert(const float* __restrict__ dq_acc,
+                                                    __nv_bfloat16* __restrict__ dq, Strides5 sdq,
+                                                    int B, int S, int H, int N) {
+  constexpr int TPR = D / 8;
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = t / TPR;
+  const int part = (int)(t % TPR);
+  if (row >= (int64_t)B * S * H * N) return;
+  const int j = (int)(row % N);
+  const int h = (int)((row / N) % H);
+  const int s = (int)((row / ((int64_t)N * H)) % S);
+  const int b = (int)(row / ((int64_t)N * H * S));
+  const float4* src = reinterpret_cast<const float4*>(dq_acc + row * D + 8 * part);
+  const float4 a = src[0], c = src[1];
+  const float f[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+  *reinterpret_cast<uint4*>(dq + sdq.at(b, s, h, j, 8 * part)) = pack8(f);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+bool tmap_rows(CUtensorMap* m, const void* base, const Strides5& st, const Problem& P) {
+  const uint64_t dims[5] = {(uint64_t)P.D, (uint64_t)P.N, (uint64_t)P.H, (uint64_t)P.S,
+                            (uint64_t)P.B};
+  const uint64_t str[4] = {(uint64_t)st.n * 2, (uint64_t)st.h * 2, (uint64_t)st.s * 2,
+                           (uint64_t)st.b * 2};
+  const uint32_t box[5] = {(uint32_t)P.D, 128, 1, 1, 1};
+  const CUtensorMapSwizzle sw =
+      P.D == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return make_tmap_bf16(m, base, 5, dims, str, box, sw);
+}
+
+bool tmap_bias(CUtensorMap* m, const void* base, const StridesBias& sb, const Problem& P,
+               bool k_contig) {
+  const uint64_t dims[4] = {(uint64_t)P.N, (uint64_t)P.N, (uint64_t)P.H, (uint64_t)P.B};
+  const uint64_t outer = k_contig ? sb.j : sb.k;
+  const uint64_t str[3] = {outer * 2, (uint64_t)sb.h * 2, (uint64_t)sb.b * 2};
+  const uint32_t box[4] = {64, 128, 1, 1};
+  return make_tmap_bf16(m, base, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, uint32_t bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D, bool KC>
+cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, const Workspace& w,
+                       unsigned int* status, cudaStream_t st, const CUtensorMap& tq,
+                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const CUtensorMap& tb) {
+  const int nt = (P.N + 127) / 128;
+  // 1) delta, dgate, dOa; zero dQ accumulator
+  {
+    PreParams pp{};
+    pp.B = P.B; pp.S = P.S; pp.H = P.H; pp.N = P.N; pp.D = D;
+    pp.out = static_cast<const __nv_bfloat16*>(a.out);
+    pp.dout = static_cast<const __nv_bfloat16*>(a.dout);
+    pp.gate = static_cast<const __nv_bfloat16*>(a.gate);
+    pp.o = P.o; pp.dO = P.dout; pp.g = P.g; pp.dg = P.dg;
+    pp.dgate = static_cast<__nv_bfloat16*>(a.dgate);
+    pp.dOa = w.dOa; pp.delta = w.delta; pp.dq_acc = w.dq_acc;
+    const int64_t threads = P.rows() * (D / 8);
+    k_pre<D><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(pp);
+  }
+  if (flags & EVOATTN_DBIAS_ATOMIC) {
+    cudaError_t e = cudaMemsetAsync(a.dbias, 0, (size_t)P.B * P.H * P.N * P.N * 4, st);
+    if (e != cudaSuccess) return e;
+  }
+  // 2) dK, dV (+ dQ partial sums)
+  {
+    using C = DkdvCfg<D>;
+    DkdvParams dp{};
+    dp.B = P.B; dp.S = P.S; dp.H = P.H; dp.N = P.N; dp.njt = nt; dp.nkt = nt;
+    dp.mask = a.mask; dp.msb = P.mask.b; dp.mss = P.mask.s; dp.msk = P.mask.k;
+    dp.lse = a.lse; dp.delta = w.delta; dp.dq_acc = w.dq_acc;
+    dp.dk = static_cast<__nv_bfloat16*>(a.dk); dp.dv = static_cast<__nv_bfloat16*>(a.dv);
+    dp.sdk = P.dk; dp.sdv = P.dv; dp.status = status;
+    auto kern = k_dkdv<D, KC>;
+    cudaError_t e = set_smem(kern, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    const uint64_t grid = (uint64_t)P.B * P.S * P.H * nt;
+    if (grid > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, 320, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, tb, dp);
+  }
+  // 3) dbias partials
+  const int slots = dbias_slots(P);
+  {
+    using C = DbiasCfg<D>;
+    DbiasParams bp{};
+    bp.B = P.B; bp.S = P.S; bp.H = P.H; bp.N = P.N; bp.njt = nt; bp.nkt = nt;
+    bp.slots = slots;
+    bp.mask = a.mask; bp.msb = P.mask.b; bp.mss = P.mask.s; bp.msk = P.mask.k;
+    bp.lse = a.lse; bp.delta = w.delta;
+    bp.atomic = (flags & EVOATTN_DBIAS_ATOMIC) ? 1 : 0;
+    bp.out = bp.atomic ? a.dbias : w.partial;
+    bp.status = status;
+    auto kern = k_dbias<D, KC>;
+    cudaError_t e = set_smem(kern, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    const uint64_t grid = (uint64_t)P.B * P.H * slots * nt * nt;
+    if (grid > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, 320, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, tb, bp);
+  }
+  // 4) ordered slot sum, dQ conversion
+  if (!(flags & EVOATTN_DBIAS_ATOMIC)) {
+    const int64_t n = (int64_t)P.B * P.H * P.N * P.N;
+    const int64_t work = (n & 3) == 0 ? n / 4 : n;
+    k_dbias_sum<<<(unsigned)((work + 255) / 256), 256, 0, st>>>(w.partial, a.dbias, n, slots);
+  }
+  {
+    const int64_t threads = P.rows() * (D / 8);
+    k_dq_convert<D><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
+        w.dq_acc, static_cast<__nv_bfloat16*>(a.dq), P.dq, P.B, P.S, P.H, P.N);
+  }
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t bwd_d(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
+                  unsigned int* status, cudaStream_t st, bool* tmap_ok) {
+  const Workspace w = carve(P, flags, ws);
+  // dOa is written dense [B,S,H,N,D]
+  const Strides5 dense{(int64_t)P.S * P.H * P.N * D, (int64_t)P.H * P.N * D, (int64_t)P.N * D,
+                       D, 1};
+  CUtensorMap tq, tk, tv, tdo, tb;
+  const bool kc = P.bias.k == 1;
+  if (!tmap_rows(&tq, a.q, P.q, P) || !tmap_rows(&tk, a.k, P.k, P) ||
+      !tmap_rows(&tv, a.v, P.v, P) || !tmap_rows(&tdo, w.dOa, dense, P) ||
+      !tmap_bias(&tb, a.bias, P.bias, P, kc)) {
+    *tmap_ok = false;
+    return cudaErrorInvalidValue;
+  }
+  return kc ? bwd_launch<D, true>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb)
+            : bwd_launch<D, false>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb);
+}
+
+}  // namespace
+
+size_t bf16_bwd_workspace_bytes(const Problem& P, unsigned flags) {
+  if (P.D != 16 && P.D != 32) return 0;
+  return carve(P, flags, nullptr).bytes;
+}
+
+cudaError_t bf16_bwd(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
+                     unsigned int* status, cudaStream_t st, bool* tmap_ok) {
+  switch (P.D) {
+    case 16: return bwd_d<16>(P, a, flags, ws, status, st, tmap_ok);
+    case 32: return bwd_d<32>(P, a, flags, ws, status, st, tmap_ok);
+  }
   return cudaErrorNotSupported;
 }
 
