@@ -1,0 +1,385 @@
+#!/usr/bin/env python3
+"""EvoAttention forward + backward benchmark on GB300.
+
+One step = evoattn_fwd + evoattn_bwd (every kernel of the path) over the
+ending-node triangle attention of the N=768 pair representation
+(B=1, S=N=768, H=4, D=32, bf16, 5 % trailing key mask, sigmoid gate), with
+the inputs already resident in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Throughput counts 4*B*S*H*N^2*D FLOP for the forward and 2.5x that for the
+backward.  With N>1 (torchrun) every rank runs its own replica of the
+workload (the path has no cross-GPU exchange); the value is the total FLOP of
+all ranks over the slowest rank's time.  `--impl reference` times the float64
+CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "EvoAttention fwd+bwd TFLOP/s and % of GB300 BF16 dense peak (N=768 triangle attn)"
+WORKLOAD = "pairformer_end_n768"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        loaded = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def config_block(w):
+    return {"workload": w.name, "B": w.B, "S": w.S, "N": w.N, "H": w.H, "D": w.D,
+            "node": w.node, "mask": f"{w.mask_tail} trailing keys masked" if w.mask == "tail"
+            else w.mask, "gate": w.gate, "global_batch": w.B * w.S, "seq_len": w.N,
+            "parallelism": "replicas", "l2": "inputs larger than L2 (no flush needed)"}
+
+
+def oracle_sample_time(w, n_rows, device_inputs=None):
+    """Time the float64 oracle (fwd + bwd) on n_rows of the workload's s rows.
+    Returns (seconds, flops_of_sample, threads)."""
+    import torch
+
+    import oracle
+    from protein_folding_attention_gb300 import synthetic
+    x = device_inputs if device_inputs is not None else synthetic.make_inputs(
+        synthetic.Workload(w.name + "_sample", B=w.B, S=n_rows, N=w.N, H=w.H, D=w.D,
+                           dtype=w.dtype, node=w.node, mask=w.mask, mask_tail=w.mask_tail,
+                           mask_p=w.mask_p, gate=w.gate, bias_std=w.bias_std, seed=w.seed))
+    sub = {k: (None if v is None else (v.cpu() if k == "bias" else v[:, :n_rows].cpu()))
+           for k, v in x.items()}
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.fwd(sub["q"], sub["k"], sub["v"], sub["bias"], sub["mask"], sub["gate"])
+    oracle.bwd(sub["q"], sub["k"], sub["v"], sub["bias"], sub["mask"], sub["gate"], sub["dout"])
+    dt = time.perf_counter() - t0
+    flops = 14 * w.B * n_rows * w.H * w.N * w.N * w.D
+    del torch
+    return dt, flops, oracle.num_threads()
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    rows = args.ref_rows
+    times = []
+    flops = threads = 0
+    if args.warmup > 0:          # one untimed sample builds the oracle and warms caches
+        oracle_sample_time(w, rows)
+    for _ in range(args.steps):
+        dt, flops, threads = oracle_sample_time(w, rows)
+        times.append(dt)
+    t = statistics.mean(times)
+    value = flops / t / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_block(w), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"{rows} of {w.S} s rows (fwd+bwd incl. dbias over them), "
+                                       f"full N={w.N}, H={w.H}, D={w.D}"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+
+    from protein_folding_attention_gb300 import evoattn, synthetic
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    evoattn.load()
+    peaks, peak_src = load_peaks()
+
+    x = synthetic.make_inputs(w, device=dev)
+    B, S, H, N, D = w.B, w.S, w.H, w.N, w.D
+    out = synthetic.empty_view(w, dev)
+    lse = torch.empty(B, S, H, N, device=dev, dtype=torch.float32)
+    grads = {n: synthetic.empty_view(w, dev) for n in ("dq", "dk", "dv", "dgate")}
+    dbias = torch.empty(B, H, N, N, device=dev, dtype=torch.float32)
+    wsp = torch.empty(evoattn.workspace_size(B, S, H, N, D, w.torch_dtype), device=dev,
+                      dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        evoattn.fwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out=out, lse=lse)
+
+    def bwd(events=None):
+        evoattn.bwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out, lse,
+                    x["dout"], dq=grads["dq"], dk=grads["dk"], dv=grads["dv"], dbias=dbias,
+                    dgate=grads["dgate"], workspace=wsp, stage_events=events)
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+
+    mem0 = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    barrier()
+    status = evoattn.device_status()
+    if status != evoattn.OK:
+        raise RuntimeError(f"device status {status} after warm-up")
+    peak_extra = torch.cuda.max_memory_allocated(dev) - mem0
+
+    # ---- timed region: K steps, per-kernel events on the launching stream ----
+    n_ev = 5
+    ev_f = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    ev_b = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+            for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        t0.record(stream)
+        for i in range(args.steps):
+            ev_f[i][0].record(stream)
+            fwd()
+            ev_f[i][1].record(stream)
+            bwd(ev_b[i])
+        t1.record(stream)
+        barrier()
+    elapsed = t0.elapsed_time(t1) * 1e-3
+    if pg is not None:
+        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed = float(t.item())
+    status = evoattn.device_status()
+    if status != evoattn.OK:
+        raise RuntimeError(f"device status {status} in timed region")
+
+    t_fwd = statistics.mean(a.elapsed_time(b) for a, b in ev_f) * 1e-3
+    stage = [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev_b) * 1e-3
+             for k in range(n_ev - 1)]
+    t_bwd = sum(stage)
+    step = elapsed / args.steps
+    total_flops = (w.fwd_flops + w.bwd_flops) * ws
+    value = total_flops / step / 1e12
+    peak = peaks["bf16_tflops"]
+
+    # ---- end to end: pinned host inputs -> device, fwd+bwd, results -> host
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: (None if v is None else torch.empty_strided(
+            v.size(), v.stride(), dtype=v.dtype, pin_memory=True).copy_(v))
+            for k, v in x.items()}
+        outs = {"out": out, "dbias": dbias, **grads}
+        host_out = {k: torch.empty_strided(v.size(), v.stride(), dtype=v.dtype,
+                                           pin_memory=True) for k, v in outs.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+        def e2e_step():
+            for k, v in host_in.items():
+                if v is not None:
+                    x[k].copy_(v, non_blocking=True)
+            fwd()
+            bwd()
+            for k, v in host_out.items():
+                v.copy_(outs[k], non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ksteps = max(3, args.steps // 2)
+        barrier()
+        e0.record(stream)
+        for _ in range(ksteps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        te = e0.elapsed_time(e1) * 1e-3 / ksteps
+        if pg is not None:
+            t = torch.tensor([te], device=dev, dtype=torch.float64)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            te = float(t.item())
+        e2e = {"value": total_flops / te / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3}
+
+    # ---- roofline of the dominant kernel --------------------------------------
+    kernels = {
+        "evoattn_fwd_kernel": (t_fwd, w.fwd_flops),
+        "k_pre": (stage[0], 0),
+        "k_dkdv": (stage[1], w.bwd_flops),
+        "k_dbias": (stage[2], 0),
+        "k_dbias_sum+k_dq_convert": (stage[3], 0),
+    }
+    dom = max(kernels, key=lambda k: kernels[k][0])
+    dt_dom, fl_dom = kernels[dom]
+    traffic = profiled_traffic(dom, w.name)
+    if fl_dom > 0:
+        achieved = fl_dom / dt_dom / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src} bf16 burst", "traffic": traffic}
+    else:
+        roof = {"kernel": dom, "bound": "alu", "achieved": None, "peak": None,
+                "unit": None, "frac": None, "traffic": traffic}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        dt, fl, thr = oracle_sample_time(w, args.cpu_rows)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+               "sample": f"{args.cpu_rows} of {w.S} s rows (fwd+bwd incl. dbias over them), "
+                         f"full N={w.N}, H={w.H}, D={w.D}; {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_block(w),
+            "fwd": {"ms": t_fwd * 1e3, "tflops": w.fwd_flops / t_fwd / 1e12,
+                    "frac_of_peak": w.fwd_flops / t_fwd / 1e12 / peak},
+            "bwd": {"ms": t_bwd * 1e3, "tflops": w.bwd_flops / t_bwd / 1e12,
+                    "frac_of_peak": w.bwd_flops / t_bwd / 1e12 / peak,
+                    "stages_ms": dict(zip(["pre", "dkdv", "dbias", "reduce"],
+                                          [s * 1e3 for s in stage]))},
+            "peak_tflops": peak, "peak_source": peak_src,
+            "frac_of_peak": value / ws / peak,
+            "peak_mem_extra_bytes": int(peak_extra),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks.summary(),
+            "gpu_launches": args.steps * 6,
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if one
+    exists for this kernel and workload (profiles/traffic.txt lines:
+    kernel workload bytes_per_launch)."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        for line in open(p):
+            f = line.split()
+            if len(f) >= 3 and f[0] == kernel and f[1] == workload:
+                return float(f[2])
+    except OSError:
+        pass
+    return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--ref-rows", type=int, default=16,
+                    help="s rows per step of the --impl reference arm")
+    ap.add_argument("--cpu-rows", type=int, default=48,
+                    help="s rows of the cpu_baseline sample")
+    ap.add_argument("--s-rows", type=int, default=0,
+                    help="profiling only: truncate the workload to this many s rows")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    from protein_folding_attention_gb300 import synthetic
+    w = synthetic.WORKLOADS[args.workload]
+    if args.s_rows:
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}_s{args.s_rows}", S=args.s_rows)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

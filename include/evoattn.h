@@ -160,6 +160,35 @@ evoattn_status evoattn_bwd(const void* q, const int64_t q_strides[5],
                            cudaStream_t stream);
 
 /*
+ * Same as evoattn_bwd, and additionally records stage_events[0..4] on
+ * `stream` around its kernels: [0] before the first kernel, [1] after the
+ * per-row preprocessing (delta, dgate, gated output gradient), [2] after the
+ * dK/dV kernel (which also accumulates dQ), [3] after the dbias kernel, [4]
+ * after the final reductions (ordered dbias sum, dQ conversion).  The events
+ * are created and owned by the caller (cudaEventCreate); elapsed times
+ * between consecutive events are the stage durations.  stage_events may not
+ * be NULL.  For profiling; the work done is identical to evoattn_bwd.
+ */
+evoattn_status evoattn_bwd_profiled(const void* q, const int64_t q_strides[5],
+                                    const void* k, const int64_t k_strides[5],
+                                    const void* v, const int64_t v_strides[5],
+                                    const void* pair_bias, const int64_t bias_strides[4],
+                                    const uint8_t* mask, const int64_t mask_strides[3],
+                                    const void* gate, const int64_t gate_strides[5],
+                                    const void* out, const int64_t out_strides[5],
+                                    const float* lse,
+                                    const void* dout, const int64_t dout_strides[5],
+                                    void* dq, const int64_t dq_strides[5],
+                                    void* dk, const int64_t dk_strides[5],
+                                    void* dv, const int64_t dv_strides[5],
+                                    float* dbias,
+                                    void* dgate, const int64_t dgate_strides[5],
+                                    int B, int S, int H, int N, int D,
+                                    evoattn_dtype dtype, unsigned flags,
+                                    void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream, cudaEvent_t stage_events[5]);
+
+/*
  * Synchronises `stream`, then reads and clears the calling device's status
  * word.  *device_status receives EVOATTN_OK, or EVOATTN_ERR_TIMEOUT when a
  * kernel enqueued since the last read gave up a bounded wait (its outputs are

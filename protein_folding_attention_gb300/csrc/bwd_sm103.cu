@@ -837,8 +837,9 @@ template <int D, bool KC>
 cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, const Workspace& w,
                        unsigned int* status, cudaStream_t st, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const CUtensorMap& tb) {
+                       const CUtensorMap& tb, cudaEvent_t* ev) {
   const int nt = (P.N + 127) / 128;
+  if (ev) cudaEventRecord(ev[0], st);
   // 1) delta, dgate, dOa; zero dQ accumulator
   {
     PreParams pp{};
@@ -856,6 +857,7 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     cudaError_t e = cudaMemsetAsync(a.dbias, 0, (size_t)P.B * P.H * P.N * P.N * 4, st);
     if (e != cudaSuccess) return e;
   }
+  if (ev) cudaEventRecord(ev[1], st);
   // 2) dK, dV (+ dQ partial sums)
   {
     using C = DkdvCfg<D>;
@@ -872,6 +874,7 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     if (grid > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, 320, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, tb, dp);
   }
+  if (ev) cudaEventRecord(ev[2], st);
   // 3) dbias partials
   const int slots = dbias_slots(P);
   {
@@ -891,6 +894,7 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     if (grid > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, 320, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, tb, bp);
   }
+  if (ev) cudaEventRecord(ev[3], st);
   // 4) ordered slot sum, dQ conversion
   if (!(flags & EVOATTN_DBIAS_ATOMIC)) {
     const int64_t n = (int64_t)P.B * P.H * P.N * P.N;
@@ -902,12 +906,13 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     k_dq_convert<D><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
         w.dq_acc, static_cast<__nv_bfloat16*>(a.dq), P.dq, P.B, P.S, P.H, P.N);
   }
+  if (ev) cudaEventRecord(ev[4], st);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t bwd_d(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
-                  unsigned int* status, cudaStream_t st, bool* tmap_ok) {
+                  unsigned int* status, cudaStream_t st, bool* tmap_ok, cudaEvent_t* ev) {
   const Workspace w = carve(P, flags, ws);
   // dOa is written dense [B,S,H,N,D]
   const Strides5 dense{(int64_t)P.S * P.H * P.N * D, (int64_t)P.H * P.N * D, (int64_t)P.N * D,
@@ -920,8 +925,8 @@ cudaError_t bwd_d(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
     *tmap_ok = false;
     return cudaErrorInvalidValue;
   }
-  return kc ? bwd_launch<D, true>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb)
-            : bwd_launch<D, false>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb);
+  return kc ? bwd_launch<D, true>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb, ev)
+            : bwd_launch<D, false>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb, ev);
 }
 
 }  // namespace
@@ -932,10 +937,11 @@ size_t bf16_bwd_workspace_bytes(const Problem& P, unsigned flags) {
 }
 
 cudaError_t bf16_bwd(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
-                     unsigned int* status, cudaStream_t st, bool* tmap_ok) {
+                     unsigned int* status, cudaStream_t st, bool* tmap_ok,
+                     cudaEvent_t* events) {
   switch (P.D) {
-    case 16: return bwd_d<16>(P, a, flags, ws, status, st, tmap_ok);
-    case 32: return bwd_d<32>(P, a, flags, ws, status, st, tmap_ok);
+    case 16: return bwd_d<16>(P, a, flags, ws, status, st, tmap_ok, events);
+    case 32: return bwd_d<32>(P, a, flags, ws, status, st, tmap_ok, events);
   }
   return cudaErrorNotSupported;
 }

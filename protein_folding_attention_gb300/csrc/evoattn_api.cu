@@ -174,7 +174,7 @@ size_t evoattn_bwd_workspace_size(int B, int S, int H, int N, int D, evoattn_dty
   return dtype == EVOATTN_F32 ? f32_bwd_workspace_bytes(P) : bf16_bwd_workspace_bytes(P, flags);
 }
 
-evoattn_status evoattn_bwd(const void* q, const int64_t q_strides[5], const void* k,
+static evoattn_status bwd_impl(const void* q, const int64_t q_strides[5], const void* k,
                            const int64_t k_strides[5], const void* v,
                            const int64_t v_strides[5], const void* pair_bias,
                            const int64_t bias_strides[4], const uint8_t* mask,
@@ -187,7 +187,7 @@ evoattn_status evoattn_bwd(const void* q, const int64_t q_strides[5], const void
                            const int64_t dv_strides[5], float* dbias, void* dgate,
                            const int64_t dgate_strides[5], int B, int S, int H, int N, int D,
                            evoattn_dtype dtype, unsigned flags, void* workspace,
-                           size_t workspace_bytes, cudaStream_t stream) {
+                           size_t workspace_bytes, cudaStream_t stream, cudaEvent_t* events) {
   if (!q || !k || !v || !pair_bias || !out || !lse || !dout || !dq || !dk || !dv || !dbias)
     return EVOATTN_ERR_INVALID_ARG;
   if (!q_strides || !k_strides || !v_strides || !bias_strides || !out_strides ||
@@ -242,16 +242,58 @@ evoattn_status evoattn_bwd(const void* q, const int64_t q_strides[5], const void
     a.lse = const_cast<float*>(lse);
     a.dq = static_cast<float*>(dq); a.dk = static_cast<float*>(dk);
     a.dv = static_cast<float*>(dv); a.dbias = dbias; a.dgate = static_cast<float*>(dgate);
-    return cuda_status(f32_bwd(P, a, workspace, stream));
+    return cuda_status(f32_bwd(P, a, workspace, stream, events));
   }
   Bf16Ptrs a{};
   a.q = q; a.k = k; a.v = v; a.bias = pair_bias; a.gate = gate; a.mask = mask;
   a.dout = dout; a.out = const_cast<void*>(out); a.lse = const_cast<float*>(lse);
   a.dq = dq; a.dk = dk; a.dv = dv; a.dgate = dgate; a.dbias = dbias;
   bool tmap_ok = true;
-  cudaError_t e = bf16_bwd(P, a, flags, workspace, status, stream, &tmap_ok);
+  cudaError_t e = bf16_bwd(P, a, flags, workspace, status, stream, &tmap_ok, events);
   if (!tmap_ok) return EVOATTN_ERR_ALIGNMENT;
   return cuda_status(e);
+}
+
+evoattn_status evoattn_bwd(const void* q, const int64_t q_strides[5], const void* k,
+                           const int64_t k_strides[5], const void* v,
+                           const int64_t v_strides[5], const void* pair_bias,
+                           const int64_t bias_strides[4], const uint8_t* mask,
+                           const int64_t mask_strides[3], const void* gate,
+                           const int64_t gate_strides[5], const void* out,
+                           const int64_t out_strides[5], const float* lse, const void* dout,
+                           const int64_t dout_strides[5], void* dq,
+                           const int64_t dq_strides[5], void* dk,
+                           const int64_t dk_strides[5], void* dv,
+                           const int64_t dv_strides[5], float* dbias, void* dgate,
+                           const int64_t dgate_strides[5], int B, int S, int H, int N, int D,
+                           evoattn_dtype dtype, unsigned flags, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  return bwd_impl(q, q_strides, k, k_strides, v, v_strides, pair_bias, bias_strides, mask,
+                  mask_strides, gate, gate_strides, out, out_strides, lse, dout, dout_strides,
+                  dq, dq_strides, dk, dk_strides, dv, dv_strides, dbias, dgate, dgate_strides,
+                  B, S, H, N, D, dtype, flags, workspace, workspace_bytes, stream, nullptr);
+}
+
+evoattn_status evoattn_bwd_profiled(const void* q, const int64_t q_strides[5], const void* k,
+                                    const int64_t k_strides[5], const void* v,
+                                    const int64_t v_strides[5], const void* pair_bias,
+                                    const int64_t bias_strides[4], const uint8_t* mask,
+                                    const int64_t mask_strides[3], const void* gate,
+                                    const int64_t gate_strides[5], const void* out,
+                                    const int64_t out_strides[5], const float* lse,
+                                    const void* dout, const int64_t dout_strides[5], void* dq,
+                                    const int64_t dq_strides[5], void* dk,
+                                    const int64_t dk_strides[5], void* dv,
+                                    const int64_t dv_strides[5], float* dbias, void* dgate,
+                                    const int64_t dgate_strides[5], int B, int S, int H, int N,
+                                    int D, evoattn_dtype dtype, unsigned flags,
+                                    void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream, cudaEvent_t stage_events[5]) {
+  if (!stage_events) return EVOATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, q_strides, k, k_strides, v, v_strides, pair_bias, bias_strides, mask,
+                  mask_strides, gate, gate_strides, out, out_strides, lse, dout, dout_strides,
+                  dq, dq_strides, dk, dk_strides, dv, dv_strides, dbias, dgate, dgate_strides,
+                  B, S, H, N, D, dtype, flags, workspace, workspace_bytes, stream, stage_events);
 }
 
 }  // extern "C"

@@ -245,19 +245,24 @@ cudaError_t fwd_f32_d(const Problem& P, const F32Ptrs& a, cudaStream_t st) {
 }
 
 template <int D>
-cudaError_t bwd_f32_d(const Problem& P, const F32Ptrs& a, float* ws, cudaStream_t st) {
+cudaError_t bwd_f32_d(const Problem& P, const F32Ptrs& a, float* ws, cudaStream_t st,
+                      cudaEvent_t* ev) {
   const int T = 128;
   float* dOa = ws;
   float* delta = ws + P.rows() * D;
+  if (ev) cudaEventRecord(ev[0], st);
   bwd_pre_f32_kernel<D><<<blocks_for(P.rows(), T), T, 0, st>>>(P, a.out, a.dout, a.gate,
                                                                 a.dgate, dOa, delta);
+  if (ev) cudaEventRecord(ev[1], st);
   bwd_dq_f32_kernel<D><<<blocks_for(P.rows(), T), T, 0, st>>>(
       P, a.q, a.k, a.v, a.bias, a.mask, a.lse, dOa, delta, a.dq);
   bwd_dkdv_f32_kernel<D><<<blocks_for(P.rows(), T), T, 0, st>>>(
       P, a.q, a.k, a.v, a.bias, a.mask, a.lse, dOa, delta, a.dk, a.dv);
+  if (ev) cudaEventRecord(ev[2], st);
   const int64_t nb = (int64_t)P.B * P.H * P.N * P.N;
   bwd_dbias_f32_kernel<D><<<blocks_for(nb, T), T, 0, st>>>(
       P, a.q, a.k, a.v, a.bias, a.mask, a.lse, dOa, delta, a.dbias);
+  if (ev) { cudaEventRecord(ev[3], st); cudaEventRecord(ev[4], st); }
   return cudaGetLastError();
 }
 
@@ -277,13 +282,14 @@ cudaError_t f32_fwd(const Problem& P, const F32Ptrs& a, cudaStream_t st) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t f32_bwd(const Problem& P, const F32Ptrs& a, void* ws, cudaStream_t st) {
+cudaError_t f32_bwd(const Problem& P, const F32Ptrs& a, void* ws, cudaStream_t st,
+                    cudaEvent_t* ev) {
   float* w = static_cast<float*>(ws);
   switch (P.D) {
-    case 16: return bwd_f32_d<16>(P, a, w, st);
-    case 32: return bwd_f32_d<32>(P, a, w, st);
-    case 64: return bwd_f32_d<64>(P, a, w, st);
-    case 128: return bwd_f32_d<128>(P, a, w, st);
+    case 16: return bwd_f32_d<16>(P, a, w, st, ev);
+    case 32: return bwd_f32_d<32>(P, a, w, st, ev);
+    case 64: return bwd_f32_d<64>(P, a, w, st, ev);
+    case 128: return bwd_f32_d<128>(P, a, w, st, ev);
   }
   return cudaErrorInvalidValue;
 }

@@ -17,6 +17,7 @@ struct F32Ptrs {
 
 size_t f32_bwd_workspace_bytes(const Problem& P);
 cudaError_t f32_fwd(const Problem& P, const F32Ptrs& a, cudaStream_t st);
-cudaError_t f32_bwd(const Problem& P, const F32Ptrs& a, void* ws, cudaStream_t st);
+cudaError_t f32_bwd(const Problem& P, const F32Ptrs& a, void* ws, cudaStream_t st,
+                    cudaEvent_t* events);
 
 }  // namespace evo

@@ -24,7 +24,9 @@ cudaError_t bf16_fwd(const Problem& P, const Bf16Ptrs& a, unsigned int* status,
                      cudaStream_t st, bool* tmap_ok);
 
 size_t bf16_bwd_workspace_bytes(const Problem& P, unsigned flags);
+// `events` (nullable): 5 caller-owned events recorded around the stages.
 cudaError_t bf16_bwd(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
-                     unsigned int* status, cudaStream_t st, bool* tmap_ok);
+                     unsigned int* status, cudaStream_t st, bool* tmap_ok,
+                     cudaEvent_t* events);
 
 }  // namespace evo

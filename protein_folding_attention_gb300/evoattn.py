@@ -52,6 +52,8 @@ def load(path: str = LIB_PATH):
                                 vp, i64p, fp, vp, i64p, vp, i64p, vp, i64p, vp, i64p, fp,
                                 vp, i64p, i, i, i, i, i, i, u, vp, sz, vp]
     lib.evoattn_bwd.restype = i
+    lib.evoattn_bwd_profiled.argtypes = lib.evoattn_bwd.argtypes + [ctypes.POINTER(vp)]
+    lib.evoattn_bwd_profiled.restype = i
     lib.evoattn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     lib.evoattn_get_device_status.restype = i
     lib.evoattn_status_string.argtypes = [i]
@@ -131,9 +133,12 @@ def workspace_size(B, S, H, N, D, dtype=torch.bfloat16, flags=DBIAS_DETERMINISTI
 
 
 def bwd(q, k, v, pair_bias, mask, gate, out, lse, dout, flags=DBIAS_DETERMINISTIC,
-        dq=None, dk=None, dv=None, dbias=None, dgate=None, workspace=None, stream=None):
+        dq=None, dk=None, dv=None, dbias=None, dgate=None, workspace=None, stream=None,
+        stage_events=None):
     """Gradients of sum(out * dout).  Returns dict dq, dk, dv (like q), dbias
-    (fp32 [B,H,N,N]) and dgate (None without a gate)."""
+    (fp32 [B,H,N,N]) and dgate (None without a gate).  `stage_events`: five
+    torch.cuda.Event recorded around the backward's kernels (see
+    evoattn_bwd_profiled)."""
     lib = load()
     B, S, H, N, D = q.shape
     mk = lambda t: t if t is not None else torch.empty((B, S, H, N, D), device=q.device,
@@ -150,13 +155,24 @@ def bwd(q, k, v, pair_bias, mask, gate, out, lse, dout, flags=DBIAS_DETERMINISTI
     need = workspace_size(B, S, H, N, D, q.dtype, flags)
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
-    st = lib.evoattn_bwd(_ptr(q), _s5(q), _ptr(k), _s5(k), _ptr(v), _s5(v),
-                         _ptr(pair_bias), _s4(pair_bias), _ptr(mask), _s3(mask),
-                         _ptr(gate), _s5(gate), _ptr(out), _s5(out), _ptr(lse),
-                         _ptr(dout), _s5(dout), _ptr(dq), _s5(dq), _ptr(dk), _s5(dk),
-                         _ptr(dv), _s5(dv), _ptr(dbias), _ptr(dgate), _s5(dgate),
-                         B, S, H, N, D, _dtype_code(q), flags, _ptr(workspace),
-                         workspace.numel() * workspace.element_size(), _stream(stream))
+    args = (_ptr(q), _s5(q), _ptr(k), _s5(k), _ptr(v), _s5(v),
+            _ptr(pair_bias), _s4(pair_bias), _ptr(mask), _s3(mask),
+            _ptr(gate), _s5(gate), _ptr(out), _s5(out), _ptr(lse),
+            _ptr(dout), _s5(dout), _ptr(dq), _s5(dq), _ptr(dk), _s5(dk),
+            _ptr(dv), _s5(dv), _ptr(dbias), _ptr(dgate), _s5(dgate),
+            B, S, H, N, D, _dtype_code(q), flags, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    if stage_events is None:
+        st = lib.evoattn_bwd(*args)
+    else:
+        if len(stage_events) != 5:
+            raise ValueError("stage_events needs 5 events")
+        cur = stream if stream is not None else torch.cuda.current_stream()
+        for e in stage_events:           # torch creates events lazily on first record
+            if not getattr(e, "cuda_event", 0):
+                e.record(cur)
+        handles = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in stage_events])
+        st = lib.evoattn_bwd_profiled(*args, handles)
     _check(st, "evoattn_bwd")
     return {"dq": dq, "dk": dk, "dv": dv, "dbias": dbias, "dgate": dgate}
 
