@@ -189,6 +189,56 @@ evoattn_status evoattn_bwd_profiled(const void* q, const int64_t q_strides[5],
                                     cudaStream_t stream, cudaEvent_t stage_events[5]);
 
 /*
+ * Capacity in bytes of the library-owned scratch that evoattn_bwd_noalloc
+ * uses in place of a caller workspace.
+ */
+#define EVOATTN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * Backward for callers that cannot allocate device memory.  There is no
+ * counterpart in the MegaFold paper; it is a deployment convenience.
+ *
+ * Some callers cannot hand the library a workspace: a plugin that runs inside
+ * a host framework which owns every device allocation and gives its plugins no
+ * allocator, or a latency-critical caller that must not call cudaMalloc
+ * (which can synchronise the device) on its hot path.  This entry point does
+ * the same work as evoattn_bwd with the same arguments, minus the workspace:
+ * its scratch lives in one statically sized device array inside the library,
+ * EVOATTN_NOALLOC_SCRATCH_BYTES large, which every GPU that loads the library
+ * holds until the process exits.  It never calls cudaMalloc, cudaFree or any
+ * allocating routine.
+ *
+ *  - Problems whose scratch need (evoattn_bwd_workspace_size for the same
+ *    arguments) exceeds EVOATTN_NOALLOC_SCRATCH_BYTES are rejected with
+ *    EVOATTN_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on a device looks up the device address of the scratch
+ *    array (with that device current); make that first call before any stream
+ *    capture begins.
+ *  - Every call on a device shares the one array and leaves its contents
+ *    behind; the kernels overwrite every scratch byte they later read, so
+ *    nothing needs clearing between calls.  Calls whose work overlaps on the
+ *    GPU (different streams, or different host threads without ordering)
+ *    race on the array and give undefined results: serialise them.
+ */
+evoattn_status evoattn_bwd_noalloc(const void* q, const int64_t q_strides[5],
+                                   const void* k, const int64_t k_strides[5],
+                                   const void* v, const int64_t v_strides[5],
+                                   const void* pair_bias, const int64_t bias_strides[4],
+                                   const uint8_t* mask, const int64_t mask_strides[3],
+                                   const void* gate, const int64_t gate_strides[5],
+                                   const void* out, const int64_t out_strides[5],
+                                   const float* lse,
+                                   const void* dout, const int64_t dout_strides[5],
+                                   void* dq, const int64_t dq_strides[5],
+                                   void* dk, const int64_t dk_strides[5],
+                                   void* dv, const int64_t dv_strides[5],
+                                   float* dbias,
+                                   void* dgate, const int64_t dgate_strides[5],
+                                   int B, int S, int H, int N, int D,
+                                   evoattn_dtype dtype, unsigned flags,
+                                   cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the calling device's status
  * word.  *device_status receives EVOATTN_OK, or EVOATTN_ERR_TIMEOUT when a
  * kernel enqueued since the last read gave up a bounded wait (its outputs are

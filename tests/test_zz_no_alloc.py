@@ -1,0 +1,79 @@
+"""evoattn_bwd_noalloc: the backward for callers that cannot allocate device
+memory (a plugin inside a framework that owns every device allocation, or a
+hot path that must not call cudaMalloc).  Its scratch is a fixed array inside
+the library instead of a caller workspace.
+
+Called through the C ABI and checked against evoattn_bwd (caller workspace)
+on the same inputs, twice in a row, since consecutive calls share the array.
+This file is collected last so that a run stopping at the first failure has
+already run every other test."""
+import ctypes
+
+import pytest
+import torch
+
+from protein_folding_attention_gb300 import evoattn, synthetic
+
+from helpers import GRAD_REL, rel_l2, to_device
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 32 << 20  # EVOATTN_NOALLOC_SCRATCH_BYTES in include/evoattn.h
+
+
+def _noalloc_fn():
+    lib = evoattn.load()
+    fn = lib.evoattn_bwd_noalloc
+    fn.argtypes = lib.evoattn_bwd.argtypes[:-3] + [ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+def _call_noalloc(fn, x, out, lse, grads, dbias):
+    s5 = lambda t: None if t is None else (ctypes.c_int64 * 5)(*t.stride())
+    p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    B, S, H, N, D = x["q"].shape
+    return fn(p(x["q"]), s5(x["q"]), p(x["k"]), s5(x["k"]), p(x["v"]), s5(x["v"]),
+              p(x["bias"]), (ctypes.c_int64 * 4)(*x["bias"].stride()),
+              p(x["mask"]), (ctypes.c_int64 * 3)(*x["mask"].stride()),
+              p(x["gate"]), s5(x["gate"]), p(out), s5(out), p(lse),
+              p(x["dout"]), s5(x["dout"]), p(grads["dq"]), s5(grads["dq"]),
+              p(grads["dk"]), s5(grads["dk"]), p(grads["dv"]), s5(grads["dv"]), p(dbias),
+              p(grads["dgate"]), s5(grads["dgate"]), B, S, H, N, D, evoattn.BF16,
+              evoattn.DBIAS_DETERMINISTIC,
+              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+@pytest.mark.parametrize("node", ["starting", "ending"])
+def test_noalloc_matches_workspace_backward_twice(node):
+    w = synthetic.small("na", B=1, S=16, N=200, H=2, D=32, dtype="bf16", node=node,
+                        mask="bernoulli", mask_p=0.2, gate=True, seed=21)
+    assert evoattn.workspace_size(w.B, w.S, w.H, w.N, w.D) <= SCRATCH_BYTES
+    x = {k: to_device(v, "cuda") for k, v in synthetic.make_inputs(w).items()}
+    out, lse = evoattn.fwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"])
+    ref = evoattn.bwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out, lse,
+                      x["dout"])
+    fn = _noalloc_fn()
+    for _ in range(2):
+        grads = {n: torch.full_like(x["q"], float("nan")) for n in ("dq", "dk", "dv", "dgate")}
+        dbias = torch.full_like(ref["dbias"], float("nan"))
+        assert _call_noalloc(fn, x, out, lse, grads, dbias) == evoattn.OK
+        assert evoattn.device_status() == evoattn.OK
+        for n in ("dq", "dk", "dv", "dgate"):
+            assert torch.isfinite(grads[n]).all()
+            assert rel_l2(grads[n], ref[n]) <= GRAD_REL, n
+        assert rel_l2(dbias, ref["dbias"]) <= GRAD_REL
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    w = synthetic.small("big", B=1, S=64, N=384, H=4, D=32, dtype="bf16", node="starting",
+                        mask="none", gate=False, seed=1)
+    assert evoattn.workspace_size(w.B, w.S, w.H, w.N, w.D) > SCRATCH_BYTES
+    x = {k: (None if v is None else to_device(v, "cuda"))
+         for k, v in synthetic.make_inputs(w).items()}
+    x["mask"] = torch.ones(w.B, w.S, w.N, dtype=torch.uint8, device="cuda")
+    out, lse = evoattn.fwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], None)
+    grads = {n: torch.empty_like(x["q"]) for n in ("dq", "dk", "dv")}
+    grads["dgate"] = None
+    dbias = torch.empty(w.B, w.H, w.N, w.N, device="cuda")
+    assert _call_noalloc(_noalloc_fn(), x, out, lse, grads, dbias) == evoattn.ERR_WORKSPACE
