@@ -175,12 +175,13 @@ __device__ __forceinline__ float bias_at(const uint8_t* tile, int j, int k) {
 // ---------------------------------------------------------------------------
 // k_dkdv
 // ---------------------------------------------------------------------------
-// Warps: 0 TMA producer, 1 MMA issuer, 2-9 two compute warpgroups.  A compute
-// thread owns key k (TMEM lane 32*(warp%4)+lane) and, of each 128-query tile,
-// the 64 queries of its warpgroup's half.  Tensor memory columns:
-//   S^T 0..127, dP^T 128..255 (fp32, lane = key), P^T 256.., dS^T 320..
-//   (bf16 pairs, 32 columns per warpgroup half), dQ partial 384.. (lane =
-//   query), dK 384+D.., dV 384+2D.. (lane = key).
+// Warps (384 threads): 0 TMA producer, 1 MMA issuer, 2-3 idle (their
+// warpgroup hands registers to the compute warpgroups), 4-11 two compute
+// warpgroups.  A compute thread owns key k (TMEM lane 32*(warp%4)+lane) and,
+// of each 128-query tile, the 64 queries of its warpgroup's half.  Tensor
+// memory columns: S^T 0..127, dP^T 128..255 (fp32, lane = key), P^T 256..,
+// dS^T 320.. (bf16 pairs, 32 columns per half), two dQ partial buffers
+// 384.. (lane = query), dK and dV after them (lane = key).
 template <int D>
 struct DkdvCfg : Tile<D> {
   using T = Tile<D>;
@@ -189,13 +190,18 @@ struct DkdvCfg : Tile<D> {
   static constexpr uint32_t OFF_V = OFF_K + T::TILE;
   static constexpr uint32_t OFF_Q = OFF_V + T::TILE;
   static constexpr uint32_t OFF_DO = OFF_Q + NQ * T::TILE;
-  static constexpr uint32_t OFF_BIAS = OFF_DO + NQ * T::TILE;
-  static constexpr uint32_t OFF_DS = OFF_BIAS + NQ * T::BIAS_TILE;
-  static constexpr uint32_t OFF_LD = OFF_DS + 128 * 128 * 2;  // lse2[128], delta[128] per stage
+  static constexpr uint32_t OFF_BIAS = OFF_DO + NQ * T::TILE;   // rows = key k
+  static constexpr uint32_t OFF_RAW = OFF_BIAS + NQ * T::BIAS_TILE;
+  static constexpr uint32_t OFF_DS = OFF_RAW + T::BIAS_TILE;
+  static constexpr uint32_t OFF_LD = OFF_DS + 128 * 128 * 2;  // lse2[128], delta/sqrt(D)[128]
   static constexpr uint32_t SMEM = OFF_LD + NQ * 256 * 4;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_P = 256, T_DS = 320, T_DQ = 384,
-                            T_DK = 384 + D, T_DV = 384 + 2 * D;
+                            T_DK = 384 + 2 * D, T_DV = 384 + 3 * D;
+  static_assert(T_DV + D <= 512, "tensor memory overflow");
+  static constexpr int THREADS = 384;
+  static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 224;
+  static_assert(REGS_LOW * 128 + REGS_HIGH * 256 <= LAUNCH_REGS * THREADS, "register split");
 };
 
 struct DkdvParams {
@@ -211,7 +217,7 @@ struct DkdvParams {
 };
 
 template <int D, bool BIAS_K_CONTIG>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     k_dkdv(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
            const __grid_constant__ CUtensorMap tm_bias, const DkdvParams p) {
@@ -220,8 +226,8 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_kv, bar_qd_full[C::NQ], bar_qd_empty[C::NQ], bar_b_full[C::NQ],
-      bar_b_empty[C::NQ], bar_s_full, bar_sdp_free, bar_p_ready, bar_mma_done, bar_dq_free,
-      bar_drain;
+      bar_b_empty[C::NQ], bar_raw, bar_s_full, bar_sdp_free, bar_p_ready, bar_mma_done,
+      bar_dq_free[2], bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -236,12 +242,16 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_kv, 1);
+    mbar_init(&bar_raw, 1);
     for (int i = 0; i < C::NQ; ++i) {
       mbar_init(&bar_qd_full[i], 1); mbar_init(&bar_qd_empty[i], 1);
       mbar_init(&bar_b_full[i], 1); mbar_init(&bar_b_empty[i], 256);
     }
     mbar_init(&bar_s_full, 1); mbar_init(&bar_sdp_free, 256); mbar_init(&bar_p_ready, 256);
-    mbar_init(&bar_mma_done, 1); mbar_init(&bar_dq_free, 256); mbar_init(&bar_drain, 1);
+    // one "read" barrier per dQ buffer: a single barrier could complete two
+    // phases (tiles jt-2 and jt-1) before the MMA thread looks at it
+    mbar_init(&bar_mma_done, 1); mbar_init(&bar_dq_free[0], 256); mbar_init(&bar_dq_free[1], 256);
+    mbar_init(&bar_drain, 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(&tmem_slot, 512);
@@ -254,33 +264,61 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_p = &abort_flag;
+  const WaitCtx wctx{abort_p, p.status};
   const int64_t row0 = (((int64_t)b * p.S + s) * p.H + h) * p.N;  // row of (b,s,h,0)
+  auto teardown = [&]() {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+    if (threadIdx.x == 0) report_abort(abort_p, p.status);
+  };
 
+  if (warp < 4) {
+  // setmaxnreg is warpgroup-aligned: one instance for warps 0-3, one for 4-11
+  regs_dec<C::REGS_LOW>();
   if (warp == 0) {
     // ============================ producer =================================
+    // The compute threads read the bias tile by key rows.  A key-row-major
+    // tile (queries contiguous: the ending-node view) is fetched straight
+    // into its stage; a query-row-major one is staged and transposed.
+    auto issue_bias = [&](int jt, uint8_t* dst, uint64_t* bar) {
+      mbar_arrive_expect_tx(bar, C::BIAS_TILE);
+      if (BIAS_K_CONTIG) {
+        tma_load_4d(dst, &tm_bias, bar, kt * 128, jt * 128, h, b);
+        tma_load_4d(dst + 16384, &tm_bias, bar, kt * 128 + 64, jt * 128, h, b);
+      } else {
+        tma_load_4d(dst, &tm_bias, bar, jt * 128, kt * 128, h, b);
+        tma_load_4d(dst + 16384, &tm_bias, bar, jt * 128 + 64, kt * 128, h, b);
+      }
+    };
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar_kv, 2 * C::TILE);
       tma_load_5d(smem + C::OFF_K, &tm_k, &bar_kv, 0, kt * 128, h, s, b);
       tma_load_5d(smem + C::OFF_V, &tm_v, &bar_kv, 0, kt * 128, h, s, b);
+      if (BIAS_K_CONTIG) issue_bias(0, smem + C::OFF_RAW, &bar_raw);
     }
+    const float inv_sqrt_d = rsqrtf((float)D);
     bool ok = true;
-    int issued = 0;
+    int issued = 0, raw_issued = BIAS_K_CONTIG ? 1 : 0;
     for (int jt = 0; jt < njt; ++jt) {
       const int st = jt % C::NQ;
       if (jt >= C::NQ) {
-        ok = mbar_wait(&bar_qd_empty[st], ((jt / C::NQ) - 1) & 1, abort_p) &&
-             mbar_wait(&bar_b_empty[st], ((jt / C::NQ) - 1) & 1, abort_p);
+        ok = mbar_wait(&bar_qd_empty[st], ((jt / C::NQ) - 1) & 1, wctx) &&
+             mbar_wait(&bar_b_empty[st], ((jt / C::NQ) - 1) & 1, wctx);
       }
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      // per-query constants of this tile: lse in log2 units (+inf beyond N so
-      // that P = 0 there) and delta
+      // per-query constants of this tile: lse in log2 units (+inf beyond N
+      // so that P = 0 there) and delta / sqrt(D)
       float* ld = reinterpret_cast<float*>(smem + C::OFF_LD + st * 1024);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int jl = e * 32 + lane, j = jt * 128 + jl;
         ld[jl] = j < p.N ? p.lse[row0 + j] * kLog2e : INFINITY;
-        ld[128 + jl] = j < p.N ? p.delta[row0 + j] : 0.f;
+        ld[128 + jl] = j < p.N ? p.delta[row0 + j] * inv_sqrt_d : 0.f;
       }
       __syncwarp();
       if (lane == 0) {
@@ -288,15 +326,21 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_5d(smem + C::OFF_Q + st * C::TILE, &tm_q, &bar_qd_full[st], 0, jt * 128, h, s, b);
         tma_load_5d(smem + C::OFF_DO + st * C::TILE, &tm_do, &bar_qd_full[st], 0, jt * 128, h, s,
                     b);
-        uint8_t* dst = smem + C::OFF_BIAS + st * C::BIAS_TILE;
-        mbar_arrive_expect_tx(&bar_b_full[st], C::BIAS_TILE);
-        if (BIAS_K_CONTIG) {
-          tma_load_4d(dst, &tm_bias, &bar_b_full[st], kt * 128, jt * 128, h, b);
-          tma_load_4d(dst + 16384, &tm_bias, &bar_b_full[st], kt * 128 + 64, jt * 128, h, b);
-        } else {
-          tma_load_4d(dst, &tm_bias, &bar_b_full[st], jt * 128, kt * 128, h, b);
-          tma_load_4d(dst + 16384, &tm_bias, &bar_b_full[st], jt * 128 + 64, kt * 128, h, b);
+      }
+      uint8_t* stage = smem + C::OFF_BIAS + st * C::BIAS_TILE;
+      if (!BIAS_K_CONTIG) {
+        if (lane == 0) issue_bias(jt, stage, &bar_b_full[st]);
+      } else {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw, jt & 1, wctx));
+        if (!ok) break;
+        transpose_tile128_bf16(smem + C::OFF_RAW, stage, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bar_b_full[st]);
+          if (jt + 1 < njt) issue_bias(jt + 1, smem + C::OFF_RAW, &bar_raw);
         }
+        raw_issued = min(jt + 2, njt);
       }
       issued = jt + 1;
     }
@@ -304,8 +348,9 @@ __global__ void __launch_bounds__(320, 1)
       volatile int no_abort = 0;
       for (int jt = max(0, issued - C::NQ); jt < issued; ++jt) {
         mbar_wait(&bar_qd_full[jt % C::NQ], (jt / C::NQ) & 1, &no_abort);
-        mbar_wait(&bar_b_full[jt % C::NQ], (jt / C::NQ) & 1, &no_abort);
+        if (!BIAS_K_CONTIG) mbar_wait(&bar_b_full[jt % C::NQ], (jt / C::NQ) & 1, &no_abort);
       }
+      if (BIAS_K_CONTIG && raw_issued > 0) mbar_wait(&bar_raw, (raw_issued - 1) & 1, &no_abort);
       mbar_wait(&bar_kv, 0, &no_abort);
     }
     __syncwarp();
@@ -318,10 +363,10 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t sk = smem_u32(smem + C::OFF_K), sv = smem_u32(smem + C::OFF_V),
                      sq = smem_u32(smem + C::OFF_Q), sdo = smem_u32(smem + C::OFF_DO),
                      sds = smem_u32(smem + C::OFF_DS);
-      bool ok = mbar_wait(&bar_kv, 0, abort_p);
+      bool ok = mbar_wait(&bar_kv, 0, wctx);
       auto issue_sdp = [&](int jt) -> bool {
         const int st = jt % C::NQ;
-        if (!mbar_wait(&bar_qd_full[st], (jt / C::NQ) & 1, abort_p)) return false;
+        if (!mbar_wait(&bar_qd_full[st], (jt / C::NQ) & 1, wctx)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -338,12 +383,13 @@ __global__ void __launch_bounds__(320, 1)
         const int st = jt % C::NQ;
         // S/dP of jt are in registers: the next tile may overwrite them
         if (jt + 1 < njt) {
-          ok = mbar_wait(&bar_sdp_free, jt & 1, abort_p);
+          ok = mbar_wait(&bar_sdp_free, jt & 1, wctx);
           if (ok) ok = issue_sdp(jt + 1);
           if (!ok) break;
         }
-        ok = mbar_wait(&bar_p_ready, jt & 1, abort_p);
-        if (ok && jt > 0) ok = mbar_wait(&bar_dq_free, (jt - 1) & 1, abort_p);
+        ok = mbar_wait(&bar_p_ready, jt & 1, wctx);
+        // the dQ buffer of this tile was last read for tile jt-2
+        if (ok && jt >= 2) ok = mbar_wait(&bar_dq_free[jt & 1], ((jt >> 1) - 1) & 1, wctx);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -359,7 +405,7 @@ __global__ void __launch_bounds__(320, 1)
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K dimension = keys)
-          umma_ss(tmem + C::T_DQ, umma_desc(sds + kk * 2048, 16384, 1024, kSw128),
+          umma_ss(tmem + C::T_DQ + (jt & 1) * D, umma_desc(sds + kk * 2048, 16384, 1024, kSw128),
                   umma_desc(sk + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_q, kk > 0);
         umma_commit(&bar_qd_empty[st]);
         umma_commit(&bar_mma_done);
@@ -369,9 +415,13 @@ __global__ void __launch_bounds__(320, 1)
       mbar_wait(&bar_drain, 0, &no_abort);
     }
     __syncwarp();
+  }
+  // warps 2-3 have no role
+  teardown();
   } else {
     // ============================ compute ==================================
-    const int wg = (warp - 2) >> 2;
+    regs_inc<C::REGS_HIGH>();
+    const int wg = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int kl = quad * 32 + lane;          // key within the tile (TMEM lane)
     const int kg = kt * 128 + kl;             // key index
@@ -383,12 +433,38 @@ __global__ void __launch_bounds__(320, 1)
     if (kg >= p.N) madd = -INFINITY;
     else if (p.mask && !p.mask[b * p.msb + (int64_t)s * p.mss + (int64_t)kg * p.msk])
       madd = kMaskBias * kLog2e;
+    const float2 c1c1 = make_float2(c1, c1), l2l2 = make_float2(kLog2e, kLog2e),
+                 mm = make_float2(madd, madd), isd = make_float2(inv_sqrt_d, inv_sqrt_d);
+    // dQ partial of tile t: lane = query; this warpgroup adds half of D
+    auto dq_epilogue = [&](int t) {
+      uint32_t q16[D / 2];
+      if constexpr (D == 32) {
+        tmem_ld16(lane_base + C::T_DQ + (t & 1) * D + 16 * wg,
+                  *reinterpret_cast<uint32_t(*)[16]>(&q16[0]));
+      } else {
+        uint32_t tmp[16];
+        tmem_ld16(lane_base + C::T_DQ + (t & 1) * D, tmp);  // D = 16: each half adds 8
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q16[e] = tmp[8 * wg + e];
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bar_dq_free[t & 1]);
+      const int jg = t * 128 + kl;  // this lane's query row
+      if (jg < p.N) {
+        float* dst = p.dq_acc + (row0 + jg) * D + (D / 2) * wg;
+#pragma unroll
+        for (int e = 0; e < D / 2; e += 4)
+          red_add_v4(dst + e, __uint_as_float(q16[e]), __uint_as_float(q16[e + 1]),
+                     __uint_as_float(q16[e + 2]), __uint_as_float(q16[e + 3]));
+      }
+    };
     bool ok = true;
     for (int jt = 0; jt < njt; ++jt) {
       const int st = jt % C::NQ;
-      ok = mbar_wait(&bar_s_full, jt & 1, abort_p) &&
-           mbar_wait(&bar_qd_full[st], (jt / C::NQ) & 1, abort_p) &&
-           mbar_wait(&bar_b_full[st], (jt / C::NQ) & 1, abort_p);
+      ok = mbar_wait(&bar_s_full, jt & 1, wctx) &&
+           mbar_wait(&bar_qd_full[st], (jt / C::NQ) & 1, wctx) &&
+           mbar_wait(&bar_b_full[st], (jt / C::NQ) & 1, wctx);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -402,32 +478,43 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(&bar_sdp_free);
       const float* ld = reinterpret_cast<const float*>(smem + C::OFF_LD + st * 1024);
-      const uint8_t* btile = smem + C::OFF_BIAS + st * C::BIAS_TILE;
+      // bias row of this key, this warpgroup's 64 queries (one 64-wide box)
+      const uint8_t* brow = smem + C::OFF_BIAS + st * C::BIAS_TILE + wg * 16384 + kl * 128;
       uint32_t pk[32], dk2[32];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {  // 4 queries per step
-        const float4 l4 = *reinterpret_cast<const float4*>(ld + 64 * wg + 4 * c);
-        const float4 d4 = *reinterpret_cast<const float4*>(ld + 128 + 64 * wg + 4 * c);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pv[4], dsv[4];
+      for (int c = 0; c < 8; ++c) {  // 8 queries per step
+        const uint4 w4 = *reinterpret_cast<const uint4*>(brow + ((c ^ (kl & 7)) << 4));
+        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+        const float4 la = *reinterpret_cast<const float4*>(ld + 64 * wg + 8 * c);
+        const float4 lb = *reinterpret_cast<const float4*>(ld + 64 * wg + 8 * c + 4);
+        const float4 da = *reinterpret_cast<const float4*>(ld + 128 + 64 * wg + 8 * c);
+        const float4 db = *reinterpret_cast<const float4*>(ld + 128 + 64 * wg + 8 * c + 4);
+        const float2 nl[4] = {make_float2(-la.x, -la.y), make_float2(-la.z, -la.w),
+                              make_float2(-lb.x, -lb.y), make_float2(-lb.z, -lb.w)};
+        const float2 nd[4] = {make_float2(-da.x, -da.y), make_float2(-da.z, -da.w),
+                              make_float2(-db.x, -db.y), make_float2(-db.z, -db.w)};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int jl = 64 * wg + 4 * c + e;
-          const float bias = bias_at<BIAS_K_CONTIG>(btile, jl, kl);
-          float t = fmaf(__uint_as_float(sx[4 * c + e]), c1, madd);
-          t = fmaf(bias, kLog2e, t);
-          pv[e] = ex2(t - lv[e]);
-          dsv[e] = pv[e] * (__uint_as_float(dpx[4 * c + e]) - dv[e]) * inv_sqrt_d;
+          const int j2 = 8 * c + 2 * e;
+          float2 t = fma2(make_float2(__uint_as_float(sx[j2]), __uint_as_float(sx[j2 + 1])),
+                          c1c1, mm);
+          t = fma2(make_float2(bf16lo(wv[e]), bf16hi(wv[e])), l2l2, t);
+          t = add2(t, nl[e]);
+          const float2 pr = make_float2(ex2(t.x), ex2(t.y));
+          const float2 g = fma2(make_float2(__uint_as_float(dpx[j2]), __uint_as_float(dpx[j2 + 1])),
+                                isd, nd[e]);
+          const float2 ds = mul2(pr, g);
+          pk[4 * c + e] = pack_bf16(pr.x, pr.y);
+          dk2[4 * c + e] = pack_bf16(ds.x, ds.y);
         }
-        pk[2 * c] = pack_bf16(pv[0], pv[1]);
-        pk[2 * c + 1] = pack_bf16(pv[2], pv[3]);
-        dk2[2 * c] = pack_bf16(dsv[0], dsv[1]);
-        dk2[2 * c + 1] = pack_bf16(dsv[2], dsv[3]);
       }
       mbar_arrive(&bar_b_empty[st]);
-      // P^T and dS^T into tensor memory (A operands of dV, dK); the previous
-      // tile's MMAs are complete (waited in the dQ step below).
+      // the previous tile's MMAs read P^T, dS^T and the dS tile: wait for them
+      if (jt > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done, (jt - 1) & 1, wctx));
+        if (!ok) break;
+        tc_fence_after();
+      }
       tmem_st32(lane_base + C::T_P + 32 * wg, pk);
       tmem_st32(lane_base + C::T_DS + 32 * wg, dk2);
       // dS into shared memory as the M-major A operand of dQ = dS K: row k,
@@ -443,32 +530,13 @@ __global__ void __launch_bounds__(320, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_p_ready);
-      // dQ partial of this (query tile, key tile): lane = query; this
-      // warpgroup adds its half of the D features.
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done, jt & 1, abort_p));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        uint32_t q16[D / 2];
-        if constexpr (D == 32) {
-          tmem_ld16(lane_base + C::T_DQ + 16 * wg, *reinterpret_cast<uint32_t(*)[16]>(&q16[0]));
-        } else {
-          uint32_t tmp[16];
-          tmem_ld16(lane_base + C::T_DQ, tmp);  // D = 16: both halves read, each adds 8
-#pragma unroll
-          for (int e = 0; e < 8; ++e) q16[e] = tmp[8 * wg + e];
-        }
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bar_dq_free);
-        const int jg = jt * 128 + kl;  // this lane's query row
-        if (jg < p.N) {
-          float* dst = p.dq_acc + (row0 + jg) * D + (D / 2) * wg;
-#pragma unroll
-          for (int e = 0; e < D / 2; e += 4)
-            red_add_v4(dst + e, __uint_as_float(q16[e]), __uint_as_float(q16[e + 1]),
-                       __uint_as_float(q16[e + 2]), __uint_as_float(q16[e + 3]));
-        }
+      if (jt > 0) dq_epilogue(jt - 1);   // its MMAs completed (waited above)
+    }
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done, (njt - 1) & 1, wctx));
+      if (ok) {
+        tc_fence_after();
+        dq_epilogue(njt - 1);
       }
     }
     // ---- dK (warpgroup 0) and dV (warpgroup 1) of this key tile -----------
@@ -491,24 +559,19 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
+    teardown();
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-  if (threadIdx.x == 0) report_abort(abort_p, p.status);
 }
 
 // ---------------------------------------------------------------------------
 // k_dbias
 // ---------------------------------------------------------------------------
-// CTA = (b, h, query tile jt, key tile kt, s-slot).  Warps: 0 producer, 1 MMA,
-// 2-9 two compute warpgroups; a compute thread owns query j (TMEM lane) and
-// the 64 keys of its warpgroup's half.  Tensor memory: S 0..127, dP
-// 128..255, dbias accumulator 256..383 (fp32, lane = query).
+// CTA = (b, h, query tile jt, key tile kt, s-slot).  Warps (384 threads): 0
+// producer, 1 MMA, 2-3 idle, 4-11 two compute warpgroups; a compute thread
+// owns query j (TMEM lane) and the 64 keys of its warpgroup's half.  Tensor
+// memory: S 0..127, dP 128..255, dbias accumulator 256..383 (fp32, lane =
+// query).  The bias tile is fetched once per CTA with query rows (transposed
+// in shared memory when the view has queries contiguous).
 template <int D>
 struct DbiasCfg : Tile<D> {
   using T = Tile<D>;
@@ -518,10 +581,14 @@ struct DbiasCfg : Tile<D> {
   static constexpr uint32_t OFF_K = OFF_DO + NST * T::TILE;
   static constexpr uint32_t OFF_V = OFF_K + NST * T::TILE;
   static constexpr uint32_t OFF_BIAS = OFF_V + NST * T::TILE;
-  static constexpr uint32_t OFF_MADD = OFF_BIAS + T::BIAS_TILE;
+  static constexpr uint32_t OFF_RAW = OFF_BIAS + T::BIAS_TILE;
+  static constexpr uint32_t OFF_MADD = OFF_RAW + T::BIAS_TILE;
   static constexpr uint32_t SMEM = OFF_MADD + NST * 128 * 4;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_ACC = 256;
+  static constexpr int THREADS = 384;
+  static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 224;
+  static_assert(REGS_LOW * 128 + REGS_HIGH * 256 <= LAUNCH_REGS * THREADS, "register split");
 };
 
 struct DbiasParams {
@@ -536,7 +603,7 @@ struct DbiasParams {
 };
 
 template <int D, bool BIAS_K_CONTIG>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     k_dbias(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
             const __grid_constant__ CUtensorMap tm_bias, const DbiasParams p) {
@@ -544,8 +611,8 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t bar_bias, bar_full[C::NST], bar_empty[C::NST], bar_s_full, bar_sdp_free,
-      bar_drain;
+  __shared__ uint64_t bar_bias, bar_raw, bar_full[C::NST], bar_empty[C::NST], bar_s_full,
+      bar_sdp_free, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -564,6 +631,7 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_bias, 1);
+    mbar_init(&bar_raw, 1);
     // a stage is empty once its MMAs completed (one commit) and both compute
     // warpgroups are done with its key mask (256 arrivals)
     for (int i = 0; i < C::NST; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_empty[i], 257); }
@@ -580,25 +648,39 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_p = &abort_flag;
+  const WaitCtx wctx{abort_p, p.status};
+  auto teardown = [&]() {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+    if (threadIdx.x == 0) report_abort(abort_p, p.status);
+  };
 
+  if (warp < 4) {
+  // setmaxnreg is warpgroup-aligned: one instance for warps 0-3, one for 4-11
+  regs_dec<C::REGS_LOW>();
   if (warp == 0) {
     // ============================ producer =================================
+    bool ok = true;
     if (lane == 0) {
-      uint8_t* dst = smem + C::OFF_BIAS;
-      mbar_arrive_expect_tx(&bar_bias, C::BIAS_TILE);
+      uint8_t* dst = smem + (BIAS_K_CONTIG ? C::OFF_BIAS : C::OFF_RAW);
+      uint64_t* bar = BIAS_K_CONTIG ? &bar_bias : &bar_raw;
+      mbar_arrive_expect_tx(bar, C::BIAS_TILE);
       if (BIAS_K_CONTIG) {
-        tma_load_4d(dst, &tm_bias, &bar_bias, kt * 128, jt * 128, h, b);
-        tma_load_4d(dst + 16384, &tm_bias, &bar_bias, kt * 128 + 64, jt * 128, h, b);
+        tma_load_4d(dst, &tm_bias, bar, kt * 128, jt * 128, h, b);
+        tma_load_4d(dst + 16384, &tm_bias, bar, kt * 128 + 64, jt * 128, h, b);
       } else {
-        tma_load_4d(dst, &tm_bias, &bar_bias, jt * 128, kt * 128, h, b);
-        tma_load_4d(dst + 16384, &tm_bias, &bar_bias, jt * 128 + 64, kt * 128, h, b);
+        tma_load_4d(dst, &tm_bias, bar, jt * 128, kt * 128, h, b);
+        tma_load_4d(dst + 16384, &tm_bias, bar, jt * 128 + 64, kt * 128, h, b);
       }
     }
-    bool ok = true;
     int issued = 0;
     for (int i = 0; i < ns; ++i) {
       const int st = i % C::NST, s = s_begin + i;
-      if (i >= C::NST) ok = mbar_wait(&bar_empty[st], ((i / C::NST) - 1) & 1, abort_p);
+      if (i >= C::NST) ok = mbar_wait(&bar_empty[st], ((i / C::NST) - 1) & 1, wctx);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       float* madd = reinterpret_cast<float*>(smem + C::OFF_MADD + st * 512);
@@ -620,12 +702,20 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_5d(smem + C::OFF_V + st * C::TILE, &tm_v, &bar_full[st], 0, kt * 128, h, s, b);
       }
       issued = i + 1;
+      if (!BIAS_K_CONTIG && i == 0) {
+        // query-contiguous bias: transpose the staged tile into query rows
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw, 0, wctx));
+        if (!ok) break;
+        transpose_tile128_bf16(smem + C::OFF_RAW, smem + C::OFF_BIAS, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_bias);
+      }
     }
     if (!ok && lane == 0) {
       volatile int no_abort = 0;
       for (int i = max(0, issued - C::NST); i < issued; ++i)
         mbar_wait(&bar_full[i % C::NST], (i / C::NST) & 1, &no_abort);
-      mbar_wait(&bar_bias, 0, &no_abort);
+      mbar_wait(BIAS_K_CONTIG ? &bar_bias : &bar_raw, 0, &no_abort);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -637,8 +727,8 @@ __global__ void __launch_bounds__(320, 1)
       bool ok = true;
       for (int i = 0; i < ns && ok; ++i) {
         const int st = i % C::NST;
-        ok = mbar_wait(&bar_full[st], (i / C::NST) & 1, abort_p);
-        if (ok && i > 0) ok = mbar_wait(&bar_sdp_free, (i - 1) & 1, abort_p);
+        ok = mbar_wait(&bar_full[st], (i / C::NST) & 1, wctx);
+        if (ok && i > 0) ok = mbar_wait(&bar_sdp_free, (i - 1) & 1, wctx);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -656,24 +746,31 @@ __global__ void __launch_bounds__(320, 1)
       mbar_wait(&bar_drain, 0, &no_abort);
     }
     __syncwarp();
+  }
+  // warps 2-3 have no role
+  teardown();
   } else {
     // ============================ compute ==================================
-    const int wg = (warp - 2) >> 2;
+    regs_inc<C::REGS_HIGH>();
+    const int wg = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int jl = quad * 32 + lane;
     const int jg = jt * 128 + jl;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const float c1 = kLog2e * rsqrtf((float)D);
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_bias, 0, abort_p));
-    const uint8_t* btile = smem + C::OFF_BIAS;
+    const float2 c1c1 = make_float2(c1, c1), l2l2 = make_float2(kLog2e, kLog2e);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_bias, 0, wctx));
+    // this query's 64 bias values (one 64-wide box), query-row layout
+    const uint8_t* brow = smem + C::OFF_BIAS + wg * 16384 + jl * 128;
     for (int i = 0; i < ns && ok; ++i) {
       const int st = i % C::NST, s = s_begin + i;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, i & 1, abort_p));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, i & 1, wctx));
       if (!ok) break;
       tc_fence_after();
       const int64_t row = (((int64_t)b * p.S + s) * p.H + h) * p.N + jg;
       const float lse2 = jg < p.N ? p.lse[row] * kLog2e : INFINITY;
       const float dl = jg < p.N ? p.delta[row] : 0.f;
+      const float2 nl = make_float2(-lse2, -lse2), nd = make_float2(-dl, -dl);
       const float* madd = reinterpret_cast<const float*>(smem + C::OFF_MADD + st * 512);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -688,27 +785,28 @@ __global__ void __launch_bounds__(320, 1)
           mbar_arrive(&bar_sdp_free);
         }
 #pragma unroll
-        for (int c = 0; c < 32; c += 8) {
-          const int k0 = 64 * wg + 32 * half + c;  // key within the tile
-          float bv[8];
-          if (BIAS_K_CONTIG) {
-            const uint4 w4 = *reinterpret_cast<const uint4*>(
-                btile + (k0 >> 6) * 16384 + jl * 128 + ((((k0 & 63) >> 3) ^ (jl & 7)) << 4));
-            unpack8(w4, bv);
-          } else {
+        for (int c = 0; c < 4; ++c) {
+          const int cc = 4 * half + c;  // 16-byte chunk: keys 64*wg + 8*cc ..
+          const uint4 w4 = *reinterpret_cast<const uint4*>(brow + ((cc ^ (jl & 7)) << 4));
+          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+          const float4 ma = *reinterpret_cast<const float4*>(madd + 64 * wg + 8 * cc);
+          const float4 mb = *reinterpret_cast<const float4*>(madd + 64 * wg + 8 * cc + 4);
+          const float2 mv[4] = {make_float2(ma.x, ma.y), make_float2(ma.z, ma.w),
+                                make_float2(mb.x, mb.y), make_float2(mb.z, mb.w)};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) bv[e] = bias_at<false>(btile, jl, k0 + e);
-          }
-          const float4 m4a = *reinterpret_cast<const float4*>(madd + k0);
-          const float4 m4b = *reinterpret_cast<const float4*>(madd + k0 + 4);
-          const float mv[8] = {m4a.x, m4a.y, m4a.z, m4a.w, m4b.x, m4b.y, m4b.z, m4b.w};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float t = fmaf(__uint_as_float(sx[c + e]), c1, mv[e]);
-            t = fmaf(bv[e], kLog2e, t);
-            const float pr = ex2(t - lse2);
-            const float ds = pr * (__uint_as_float(dpx[c + e]) - dl);
-            a[c + e] = __float_as_uint(i > 0 ? __uint_as_float(a[c + e]) + ds : ds);
+          for (int e = 0; e < 4; ++e) {
+            const int k2 = 8 * c + 2 * e;
+            float2 t = fma2(make_float2(__uint_as_float(sx[k2]), __uint_as_float(sx[k2 + 1])),
+                            c1c1, mv[e]);
+            t = fma2(make_float2(bf16lo(wv[e]), bf16hi(wv[e])), l2l2, t);
+            t = add2(t, nl);
+            const float2 pr = make_float2(ex2(t.x), ex2(t.y));
+            const float2 g =
+                add2(make_float2(__uint_as_float(dpx[k2]), __uint_as_float(dpx[k2 + 1])), nd);
+            float2 ds = mul2(pr, g);
+            if (i > 0) ds = add2(ds, make_float2(__uint_as_float(a[k2]), __uint_as_float(a[k2 + 1])));
+            a[k2] = __float_as_uint(ds.x);
+            a[k2 + 1] = __float_as_uint(ds.y);
           }
         }
         tmem_st32(lane_base + col, a);
@@ -750,15 +848,8 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
+    teardown();
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-  if (threadIdx.x == 0) report_abort(abort_p, p.status);
 }
 
 // ---------------------------------------------------------------------------
@@ -833,6 +924,17 @@ cudaError_t set_smem(K kern, uint32_t bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+// A kernel that splits registers between warpgroups (setmaxnreg) must be
+// launched with at least the per-thread count the split was sized for, or its
+// raising warpgroups would wait forever: refuse to launch otherwise.
+template <typename K>
+cudaError_t check_regs(K kern, int launch_regs) {
+  cudaFuncAttributes fa{};
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  return fa.numRegs >= launch_regs ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 template <int D, bool KC>
 cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, const Workspace& w,
                        unsigned int* status, cudaStream_t st, const CUtensorMap& tq,
@@ -870,9 +972,11 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     auto kern = k_dkdv<D, KC>;
     cudaError_t e = set_smem(kern, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
+    e = check_regs(kern, C::LAUNCH_REGS);
+    if (e != cudaSuccess) return e;
     const uint64_t grid = (uint64_t)P.B * P.S * P.H * nt;
     if (grid > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, 320, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, tb, dp);
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, tb, dp);
   }
   if (ev) cudaEventRecord(ev[2], st);
   // 3) dbias partials
@@ -890,9 +994,11 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     auto kern = k_dbias<D, KC>;
     cudaError_t e = set_smem(kern, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
+    e = check_regs(kern, C::LAUNCH_REGS);
+    if (e != cudaSuccess) return e;
     const uint64_t grid = (uint64_t)P.B * P.H * slots * nt * nt;
     if (grid > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, 320, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, tb, bp);
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, tb, bp);
   }
   if (ev) cudaEventRecord(ev[3], st);
   // 4) ordered slot sum, dQ conversion

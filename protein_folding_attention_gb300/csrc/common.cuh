@@ -74,27 +74,55 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Where a bounded wait reports a give-up: the CTA's shared abort flag (so the
+// CTA's other roles stop at once) and the device status word (so every other
+// CTA of the grid gives up at its next slow-path poll instead of waiting out
+// its own limit).
+struct WaitCtx {
+  volatile int* abort_flag;        // shared memory
+  volatile unsigned int* status;   // global device status word (may be null)
+};
+
 // Report a raised abort flag to the host-visible status word.
 __device__ __forceinline__ void report_abort(volatile int* abort_flag, unsigned int* status) {
   if (*abort_flag && status) atomicOr(status, 1u << EVOATTN_ERR_TIMEOUT);
 }
 
-// Bounded wait for the phase with the given parity to complete.  `abort_flag`
-// (shared memory) is raised by whichever thread of the CTA gives up first so
-// that the others stop waiting at once.  Returns false on give-up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag) {
+// Bounded wait for the phase with the given parity to complete.  Returns
+// false on give-up (own limit reached, or another thread/CTA gave up).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   const uint32_t a = smem_u32(bar);
 #pragma unroll 1
   for (int i = 0; i < 32; ++i)
     if (mbar_try_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
 #pragma unroll 1
+  for (uint32_t n = 0;; ++n) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (*w.abort_flag) return false;
+    if ((n & 63) == 0 && w.status && (*w.status & (1u << EVOATTN_ERR_TIMEOUT))) {
+      *w.abort_flag = 1;
+      return false;
+    }
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      *w.abort_flag = 1;
+      if (w.status) atomicOr(const_cast<unsigned int*>(w.status), 1u << EVOATTN_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Bounded wait used while winding down after a give-up (for copies and MMAs
+// already issued, which complete by themselves): no early exit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* local_flag) {
+  const uint32_t a = smem_u32(bar);
+  const unsigned long long t0 = globaltimer_ns();
+#pragma unroll 1
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
-    if (abort_flag && *abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-      if (abort_flag) *abort_flag = 1;
+      *local_flag = 1;
       return false;
     }
   }
@@ -282,5 +310,79 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+}  // namespace evo
+
+namespace evo {
+
+// ---------------------------------------------------------------------------
+// 128x128 bf16 tile transpose in shared memory (one warp).
+// ---------------------------------------------------------------------------
+// Both tiles use the layout the TMA writes for a 128-row x 128-column bf16
+// tile fetched as two 64-column boxes with a 128-byte swizzle: element
+// (r, c) lives at  (c / 64) * 16384 + r * 128 + (((c % 64) / 8) ^ (r % 8)) * 16
+// + (c % 8) * 2.  dst(c, r) = src(r, c).  Each 8x8 block is read with
+// ldmatrix.trans (rows r of the source) and written with stmatrix (rows c of
+// the destination); 64 x4 instructions of each move the whole tile.
+__device__ __forceinline__ uint32_t swz128_chunk(uint32_t base, int r, int c8) {
+  // address of the 16-byte chunk holding columns 8*c8 .. 8*c8+7 of row r
+  return base + (uint32_t)((c8 >> 3) * 16384 + r * 128 + (((c8 & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void transpose_tile128_bf16(const void* src, void* dst, int lane) {
+  const uint32_t s = smem_u32(src), d = smem_u32(dst);
+  const int m = lane >> 3, i = lane & 7;  // matrix of this lane's address, row within it
+#pragma unroll 4
+  for (int it = 0; it < 64; ++it) {
+    const int blk = it * 4 + m;            // 256 8x8 blocks
+    const int rb = blk >> 4, cb = blk & 15;
+    uint32_t r0, r1, r2, r3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(swz128_chunk(s, rb * 8 + i, cb)));
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
+                     swz128_chunk(d, cb * 8 + i, rb)),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// per-warpgroup register budget (all 128 threads of the warpgroup execute it)
+// ---------------------------------------------------------------------------
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------
+// packed fp32 pairs (sm_100+): two lanes of work per instruction
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&r);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&r);
+}
 
 }  // namespace evo

@@ -11,13 +11,14 @@
 // The key tiles kt form the outer loop and the G rows the inner loop, so each
 // 128x128 pair-bias tile is loaded into shared memory once and serves G rows.
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: Q tiles, the bias tile of each kt, K/V tiles of
 //               each (kt, s) and the additive key mask of that (s, kt)
 //   warp 1      MMA issuer (one thread): S = Q K^T into TMEM, O += P V with
 //               P read from TMEM
-//   warps 2-5   softmax warpgroup 0: rows s = 0, 2, ... of the group
-//   warps 6-9   softmax warpgroup 1: rows s = 1, 3, ...
+//   warps 2-3   idle
+//   warps 4-7   softmax warpgroup 0: rows s = 0, 2, ... of the group
+//   warps 8-11  softmax warpgroup 1: rows s = 1, 3, ...
 // A softmax thread owns one query row j (TMEM lane 32*(warp%4) + lane).
 //
 // Tensor memory (512 columns): S buffer of warpgroup w at columns 128*w (fp32
@@ -53,13 +54,18 @@ struct FwdCfg {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + G * TILE;
   static constexpr uint32_t OFF_V = OFF_K + NS * TILE;
-  static constexpr uint32_t OFF_BIAS = OFF_V + NS * TILE;
-  static constexpr uint32_t OFF_MADD = OFF_BIAS + 2 * BIAS_TILE;
+  static constexpr uint32_t OFF_BIAS = OFF_V + NS * TILE;       // 2 stages, rows = query j
+  static constexpr uint32_t OFF_RAW = OFF_BIAS + 2 * BIAS_TILE; // staging of a j-contiguous bias
+  static constexpr uint32_t OFF_MADD = OFF_RAW + BIAS_TILE;
   static constexpr uint32_t SMEM = OFF_MADD + NS * BN * 4;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
+  // tensor memory: S of warpgroup w at 128*w, P of warpgroup w at 256 + 64*w,
+  // O of row s at 384 + s*D
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t TMEM_O = 256;
-  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_P = 256;
+  static constexpr uint32_t TMEM_O = 384;
+  static constexpr int THREADS = 384;
+  static_assert(TMEM_O + G * D <= TMEM_COLS, "tensor memory overflow");
 };
 
 struct FwdParams {
@@ -76,7 +82,7 @@ struct FwdParams {
 };
 
 template <int D, bool BIAS_K_CONTIG, bool HAS_GATE>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
     evoattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
@@ -86,7 +92,8 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_q, bar_kv_full[C::NS], bar_kv_empty[C::NS], bar_bias_full[2],
-      bar_bias_empty[2], bar_s_full[2], bar_p_ready[2], bar_o_done[C::G], bar_drain;
+      bar_bias_empty[2], bar_raw, bar_s_full[2], bar_s_free[2], bar_p_ready[2], bar_p_free[2],
+      bar_o_done[C::G], bar_drain;
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
 
@@ -107,12 +114,15 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_raw, 1);
     for (int i = 0; i < C::NS; ++i) { mbar_init(&bar_kv_full[i], 1); mbar_init(&bar_kv_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_bias_full[i], 1);
       mbar_init(&bar_bias_empty[i], 128 * n_wg);
       mbar_init(&bar_s_full[i], 1);
+      mbar_init(&bar_s_free[i], 128);
       mbar_init(&bar_p_ready[i], 128);
+      mbar_init(&bar_p_free[i], 1);
     }
     for (int i = 0; i < C::G; ++i) mbar_init(&bar_o_done[i], 1);
     mbar_init(&bar_drain, 1);
@@ -128,39 +138,69 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_slot;
   volatile int* abort_p = &abort_flag;
+  const WaitCtx wctx{abort_p, p.status};
 
+  // Every role ends here: all MMAs and TMEM traffic are done once every
+  // thread has arrived, then the allocating warp frees the tensor memory.
+  auto teardown = [&]() {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    if (threadIdx.x == 0) report_abort(abort_p, p.status);
+  };
+
+  if (warp < 4) {
   if (warp == 0) {
     // =================== TMA producer (whole warp) ========================
+    // A query-row-major bias tile ([j][k], keys contiguous) goes straight to
+    // its stage; a key-row-major one (the ending-node view) lands in a
+    // staging buffer and the warp transposes it into the stage.
+    auto issue_bias = [&](int kt, uint8_t* dst, uint64_t* bar) {
+      mbar_arrive_expect_tx(bar, C::BIAS_TILE);
+      if (BIAS_K_CONTIG) {
+        tma_load_4d(dst, &tm_bias, bar, kt * C::BN, jt * C::BM, h, b);
+        tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, bar, kt * C::BN + 64, jt * C::BM, h, b);
+      } else {
+        tma_load_4d(dst, &tm_bias, bar, jt * C::BM, kt * C::BN, h, b);
+        tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, bar, jt * C::BM + 64, kt * C::BN, h, b);
+      }
+    };
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar_q, g_eff * C::TILE);
       for (int s = 0; s < g_eff; ++s)
         tma_load_5d(smem + C::OFF_Q + s * C::TILE, &tm_q, &bar_q, 0, jt * C::BM, h, s0 + s, b);
+      if (!BIAS_K_CONTIG) issue_bias(0, smem + C::OFF_RAW, &bar_raw);
     }
     bool ok = true;
-    int kv_issued = 0, bias_issued = 0;  // fills issued so far
+    int kv_issued = 0, bias_issued = 0, raw_issued = BIAS_K_CONTIG ? 0 : 1;
     for (int kt = 0; kt < nkt && ok; ++kt) {
       const int bs = kt & 1;
-      if (kt >= 2) ok = mbar_wait(&bar_bias_empty[bs], ((kt >> 1) - 1) & 1, abort_p);
+      uint8_t* stage = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
+      if (kt >= 2) ok = mbar_wait(&bar_bias_empty[bs], ((kt >> 1) - 1) & 1, wctx);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      if (lane == 0) {
-        uint8_t* dst = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
-        mbar_arrive_expect_tx(&bar_bias_full[bs], C::BIAS_TILE);
-        if (BIAS_K_CONTIG) {
-          tma_load_4d(dst, &tm_bias, &bar_bias_full[bs], kt * C::BN, jt * C::BM, h, b);
-          tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, &bar_bias_full[bs], kt * C::BN + 64,
-                      jt * C::BM, h, b);
-        } else {
-          tma_load_4d(dst, &tm_bias, &bar_bias_full[bs], jt * C::BM, kt * C::BN, h, b);
-          tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, &bar_bias_full[bs], jt * C::BM + 64,
-                      kt * C::BN, h, b);
+      if (BIAS_K_CONTIG) {
+        if (lane == 0) issue_bias(kt, stage, &bar_bias_full[bs]);
+      } else {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw, kt & 1, wctx));
+        if (!ok) break;
+        transpose_tile128_bf16(smem + C::OFF_RAW, stage, lane);
+        fence_proxy_async_smem();  // generic reads of the staging buffer before its next TMA
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bar_bias_full[bs]);
+          if (kt + 1 < nkt) issue_bias(kt + 1, smem + C::OFF_RAW, &bar_raw);
         }
+        raw_issued = min(kt + 2, nkt);
       }
       bias_issued = kt + 1;
       for (int s = 0; s < g_eff; ++s) {
         const int i = kt * g_eff + s;
         const int st = i % C::NS;
-        if (i >= C::NS) ok = mbar_wait(&bar_kv_empty[st], ((i / C::NS) - 1) & 1, abort_p);
+        if (i >= C::NS) ok = mbar_wait(&bar_kv_empty[st], ((i / C::NS) - 1) & 1, wctx);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         // additive key mask of (s, kt) in log2 units: 0 kept, -1e9*log2(e)
@@ -194,8 +234,12 @@ __global__ void __launch_bounds__(320, 1)
       volatile int no_abort = 0;
       for (int i = max(0, kv_issued - C::NS); i < kv_issued; ++i)
         mbar_wait(&bar_kv_full[i % C::NS], (i / C::NS) & 1, &no_abort);
-      for (int kt = max(0, bias_issued - 2); kt < bias_issued; ++kt)
-        mbar_wait(&bar_bias_full[kt & 1], (kt >> 1) & 1, &no_abort);
+      if (BIAS_K_CONTIG) {
+        for (int kt = max(0, bias_issued - 2); kt < bias_issued; ++kt)
+          mbar_wait(&bar_bias_full[kt & 1], (kt >> 1) & 1, &no_abort);
+      } else if (raw_issued > 0) {
+        mbar_wait(&bar_raw, (raw_issued - 1) & 1, &no_abort);
+      }
       mbar_wait(&bar_q, 0, &no_abort);
     }
     __syncwarp();
@@ -206,10 +250,10 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);    // P from TMEM, V MN-major
       const uint32_t sq = smem_u32(smem + C::OFF_Q), sk = smem_u32(smem + C::OFF_K),
                      sv = smem_u32(smem + C::OFF_V);
-      bool ok = mbar_wait(&bar_q, 0, abort_p);
+      bool ok = mbar_wait(&bar_q, 0, wctx);
       auto issue_qk = [&](int i) -> bool {
         const int s = i % g_eff, st = i % C::NS, w = s & 1;
-        if (!mbar_wait(&bar_kv_full[st], (i / C::NS) & 1, abort_p)) return false;
+        if (!mbar_wait(&bar_kv_full[st], (i / C::NS) & 1, wctx)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -218,28 +262,38 @@ __global__ void __launch_bounds__(320, 1)
         umma_commit(&bar_s_full[w]);
         return true;
       };
-      // first S tile of each warpgroup
+      // the iteration after i done by the same warpgroup (rows s of equal parity)
+      auto next_same = [&](int i) -> int {
+        for (int j = i + 1; j < total; ++j)
+          if (((j % g_eff) & 1) == ((i % g_eff) & 1)) return j;
+        return -1;
+      };
       int wg_iter[2] = {0, 0};
       if (ok) ok = issue_qk(0);
       if (ok && g_eff >= 2) ok = issue_qk(1);
       for (int i = 0; i < total && ok; ++i) {
         const int kt = i / g_eff, s = i % g_eff, st = i % C::NS, w = s & 1;
-        ok = mbar_wait(&bar_p_ready[w], wg_iter[w] & 1, abort_p);
-        if (!ok) break;
+        const uint32_t par = wg_iter[w] & 1;
         ++wg_iter[w];
+        // the next S of this warpgroup goes to TMEM after this PV (issuing it
+        // earlier would make this single thread block on one warpgroup while
+        // the other one waits for its PV)
+        const int nxt = next_same(i);
+        ok = mbar_wait(&bar_p_ready[w], par, wctx);
+        if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::TMEM_O + s * D, tmem + 128 * w + kk * 8,
+          umma_ts(tmem + C::TMEM_O + s * D, tmem + C::TMEM_P + 64 * w + kk * 8,
                   umma_desc(sv + st * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_o,
                   (kt > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bar_kv_empty[st]);
         umma_commit(&bar_o_done[s]);
-        // next iteration of the same warpgroup
-        int nxt = -1;
-        for (int j = i + 1; j < total; ++j)
-          if (((j % g_eff) & 1) == w) { nxt = j; break; }
-        if (nxt >= 0) ok = issue_qk(nxt);
+        umma_commit(&bar_p_free[w]);
+        if (nxt >= 0) {
+          ok = mbar_wait(&bar_s_free[w], par, wctx);
+          if (ok) ok = issue_qk(nxt);
+        }
       }
       // every issued MMA completes before TMEM can be released
       umma_commit(&bar_drain);
@@ -247,14 +301,18 @@ __global__ void __launch_bounds__(320, 1)
       mbar_wait(&bar_drain, 0, &no_abort);
     }
     __syncwarp();
+  }
+  // warps 2-3 have no role
+  teardown();
   } else {
     // =================== softmax warpgroups ================================
-    const int wg = (warp - 2) >> 2;                  // 0 or 1
+    const int wg = (warp - 4) >> 2;                  // 0 or 1
     const int quad = warp & 3;                       // TMEM lane quadrant
     const int row = quad * 32 + lane;                // query row within the tile
     const int j = jt * C::BM + row;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const float c1 = kLog2e * rsqrtf((float)D);      // logit scale in log2 units
+    const float2 c1c1 = make_float2(c1, c1), l2l2 = make_float2(kLog2e, kLog2e);
     float m_run[C::G / 2], l_run[C::G / 2];
 #pragma unroll
     for (int u = 0; u < C::G / 2; ++u) { m_run[u] = -INFINITY; l_run[u] = 0.f; }
@@ -262,17 +320,17 @@ __global__ void __launch_bounds__(320, 1)
     int it = 0;  // iterations done by this warpgroup
     for (int kt = 0; kt < nkt && ok; ++kt) {
       const int bs = kt & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_bias_full[bs], (kt >> 1) & 1, abort_p));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_bias_full[bs], (kt >> 1) & 1, wctx));
       if (!ok) break;
-      const uint8_t* btile = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
+      const uint8_t* brow = smem + C::OFF_BIAS + bs * C::BIAS_TILE + row * 128;
 #pragma unroll
       for (int u = 0; u < C::G / 2; ++u) {
         const int s = 2 * u + wg;
         if (s >= g_eff) break;
         const int i = kt * g_eff + s;
         const int st = i % C::NS;
-        ok = mbar_wait(&bar_kv_full[st], (i / C::NS) & 1, abort_p) &&
-             mbar_wait(&bar_s_full[wg], it & 1, abort_p);
+        ok = mbar_wait(&bar_kv_full[st], (i / C::NS) & 1, wctx) &&
+             mbar_wait(&bar_s_full[wg], it & 1, wctx);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -281,55 +339,39 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < 4; ++c)
           tmem_ld32(lane_base + 128 * wg + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bar_s_free[wg]);  // S may now be overwritten by the next QK^T
         const float* madd = reinterpret_cast<const float*>(smem + C::OFF_MADD + st * C::BN * 4);
-        float mx = -INFINITY;
+        // t = S*c1 + madd + bias*log2(e), in place; 8 independent max chains
+        float mx[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mx[e] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          float bv[8];
-          if (BIAS_K_CONTIG) {
-            const uint8_t* src = btile + (c >> 3) * (C::BIAS_TILE / 2) + row * 128 +
-                                 ((((c & 7) ^ (row & 7))) << 4);
-            const uint4 w4 = *reinterpret_cast<const uint4*>(src);
-            bv[0] = bf16lo(w4.x); bv[1] = bf16hi(w4.x); bv[2] = bf16lo(w4.y); bv[3] = bf16hi(w4.y);
-            bv[4] = bf16lo(w4.z); bv[5] = bf16hi(w4.z); bv[6] = bf16lo(w4.w); bv[7] = bf16hi(w4.w);
-          } else {
-            const int jj = row & 63;
-            const uint8_t* col = btile + (row >> 6) * (C::BIAS_TILE / 2) + (jj & 7) * 2;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int kk = c * 8 + e;
-              const uint16_t u16 = *reinterpret_cast<const uint16_t*>(
-                  col + kk * 128 + ((((jj >> 3) ^ (kk & 7))) << 4));
-              bv[e] = __uint_as_float((uint32_t)u16 << 16);
-            }
-          }
+          const uint4 w4 = *reinterpret_cast<const uint4*>(
+              brow + (c >> 3) * (C::BIAS_TILE / 2) + ((((c & 7) ^ (row & 7))) << 4));
           const float4 ma = *reinterpret_cast<const float4*>(madd + 8 * c);
           const float4 mb = *reinterpret_cast<const float4*>(madd + 8 * c + 4);
-          const float mv[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+          const float2 mv[4] = {make_float2(ma.x, ma.y), make_float2(ma.z, ma.w),
+                                make_float2(mb.x, mb.y), make_float2(mb.z, mb.w)};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float t = fmaf(__uint_as_float(x[8 * c + e]), c1, mv[e]);
-            t = fmaf(bv[e], kLog2e, t);
-            x[8 * c + e] = __float_as_uint(t);
-            mx = fmaxf(mx, t);
+          for (int e = 0; e < 4; ++e) {
+            const int k2 = 8 * c + 2 * e;
+            float2 t = fma2(make_float2(__uint_as_float(x[k2]), __uint_as_float(x[k2 + 1])),
+                            c1c1, mv[e]);
+            t = fma2(make_float2(bf16lo(wv[e]), bf16hi(wv[e])), l2l2, t);
+            x[k2] = __float_as_uint(t.x);
+            x[k2 + 1] = __float_as_uint(t.y);
+            mx[e] = fmaxf(mx[e], fmaxf(t.x, t.y));
           }
         }
-        const float m_new = fmaxf(m_run[u], mx);
+        const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        const float m_new = fmaxf(m_run[u], rmax);
         const float alpha = ex2(m_run[u] - m_new);
-        float sum = 0.f;
-        uint32_t pk[64];
-#pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const float p0 = ex2(__uint_as_float(x[2 * e]) - m_new);
-          const float p1 = ex2(__uint_as_float(x[2 * e + 1]) - m_new);
-          sum += p0 + p1;
-          pk[e] = pack_bf16(p0, p1);
-        }
-        l_run[u] = l_run[u] * alpha + sum;
-        m_run[u] = m_new;
         // rescale O of this row when its running max moved (warp-uniform)
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_done[s], (kt - 1) & 1, abort_p));
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_done[s], (kt - 1) & 1, wctx));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -342,8 +384,33 @@ __global__ void __launch_bounds__(320, 1)
             tmem_st16(lane_base + C::TMEM_O + s * D + 16 * c, o);
           }
         }
-        tmem_st32(lane_base + 128 * wg, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(lane_base + 128 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        // P of the previous iteration has been consumed by its PV
+        if (it > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_p_free[wg], (it - 1) & 1, wctx));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const float2 negm = make_float2(-m_new, -m_new);
+        float2 sum[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sum[e] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int k2 = 32 * q4 + 2 * e;
+            const float2 a = add2(make_float2(__uint_as_float(x[k2]), __uint_as_float(x[k2 + 1])),
+                                  negm);
+            const float2 pr = make_float2(ex2(a.x), ex2(a.y));
+            sum[e & 3] = add2(sum[e & 3], pr);
+            pk[e] = pack_bf16(pr.x, pr.y);
+          }
+          tmem_st16(lane_base + C::TMEM_P + 64 * wg + 16 * q4, pk);
+        }
+        const float2 s01 = add2(sum[0], sum[1]), s23 = add2(sum[2], sum[3]);
+        l_run[u] = l_run[u] * alpha + ((s01.x + s01.y) + (s23.x + s23.y));
+        m_run[u] = m_new;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar_p_ready[wg]);
@@ -358,7 +425,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int u = 0; u < C::G / 2; ++u) {
         const int s = 2 * u + wg;
         if (s >= g_eff) break;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_done[s], (nkt - 1) & 1, abort_p));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_done[s], (nkt - 1) & 1, wctx));
         if (!ok) break;
         tc_fence_after();
         float o[D];
@@ -385,30 +452,23 @@ __global__ void __launch_bounds__(320, 1)
               gv[0] = bf16lo(g4.x); gv[1] = bf16hi(g4.x); gv[2] = bf16lo(g4.y); gv[3] = bf16hi(g4.y);
               gv[4] = bf16lo(g4.z); gv[5] = bf16hi(g4.z); gv[6] = bf16lo(g4.w); gv[7] = bf16hi(g4.w);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) gv[e] = 1.0f / (1.0f + ex2(-gv[e] * kLog2e));
+              for (int e = 0; e < 8; ++e) gv[e] = inv_l / (1.0f + ex2(-gv[e] * kLog2e));
             } else {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) gv[e] = 1.0f;
+              for (int e = 0; e < 8; ++e) gv[e] = inv_l;
             }
             uint4 w4;
-            w4.x = pack_bf16(o[8 * c + 0] * inv_l * gv[0], o[8 * c + 1] * inv_l * gv[1]);
-            w4.y = pack_bf16(o[8 * c + 2] * inv_l * gv[2], o[8 * c + 3] * inv_l * gv[3]);
-            w4.z = pack_bf16(o[8 * c + 4] * inv_l * gv[4], o[8 * c + 5] * inv_l * gv[5]);
-            w4.w = pack_bf16(o[8 * c + 6] * inv_l * gv[6], o[8 * c + 7] * inv_l * gv[7]);
+            w4.x = pack_bf16(o[8 * c + 0] * gv[0], o[8 * c + 1] * gv[1]);
+            w4.y = pack_bf16(o[8 * c + 2] * gv[2], o[8 * c + 3] * gv[3]);
+            w4.z = pack_bf16(o[8 * c + 4] * gv[4], o[8 * c + 5] * gv[5]);
+            w4.w = pack_bf16(o[8 * c + 6] * gv[6], o[8 * c + 7] * gv[7]);
             *reinterpret_cast<uint4*>(dst + 8 * c) = w4;
           }
         }
       }
     }
+    teardown();
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
-  }
-  if (threadIdx.x == 0) report_abort(abort_p, p.status);
 }
 
 // 5-D tensor map of a [B,S,H,N,D] bf16 view, box = 128 rows x D.
