@@ -24,6 +24,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "layout.cuh"
 #include "sm103.h"
@@ -175,6 +177,12 @@ __device__ __forceinline__ float bias_at(const uint8_t* tile, int j, int k) {
 // ---------------------------------------------------------------------------
 // k_dkdv
 // ---------------------------------------------------------------------------
+// Persistent: one CTA per SM; work item = (b, s, h, key tile kt), items
+// blockIdx.x, blockIdx.x + gridDim.x, ...; each item loops over the query
+// tiles jt.  A global tile counter g runs across items so every ring and
+// barrier phase continues from one item to the next and the producer runs
+// ahead into the next item (K/V are double-buffered per item).
+//
 // Warps (384 threads): 0 TMA producer, 1 MMA issuer, 2-3 idle (their
 // warpgroup hands registers to the compute warpgroups), 4-11 two compute
 // warpgroups.  A compute thread owns key k (TMEM lane 32*(warp%4)+lane) and,
@@ -182,30 +190,38 @@ __device__ __forceinline__ float bias_at(const uint8_t* tile, int j, int k) {
 // memory columns: S^T 0..127, dP^T 128..255 (fp32, lane = key), P^T 256..,
 // dS^T 320.. (bf16 pairs, 32 columns per half), two dQ partial buffers
 // 384.. (lane = query), dK and dV after them (lane = key).
-template <int D>
+//
+// The MMA thread polls its barriers (mbarrier.test_wait) and issues
+// whichever is ready of: S/dP of the next tile, and dV/dK/dQ of the oldest
+// tile whose P/dS are stored, so neither waits behind the other.
+template <int D, bool BIAS_K_CONTIG>
 struct DkdvCfg : Tile<D> {
   using T = Tile<D>;
-  static constexpr int NQ = 2;  // query-tile pipeline stages
-  static constexpr uint32_t OFF_K = 0;
-  static constexpr uint32_t OFF_V = OFF_K + T::TILE;
-  static constexpr uint32_t OFF_Q = OFF_V + T::TILE;
+  static constexpr int NQ = 3;  // Q/dO/(lse,delta) stages
+  // bias stages: a key-row-major bias needs no staging buffer, which leaves
+  // room for a third stage
+  static constexpr int NB = BIAS_K_CONTIG ? 2 : 3;
+  static constexpr uint32_t OFF_K = 0;                              // 2 stages
+  static constexpr uint32_t OFF_V = OFF_K + 2 * T::TILE;            // 2 stages
+  static constexpr uint32_t OFF_Q = OFF_V + 2 * T::TILE;
   static constexpr uint32_t OFF_DO = OFF_Q + NQ * T::TILE;
-  static constexpr uint32_t OFF_BIAS = OFF_DO + NQ * T::TILE;   // rows = key k
-  static constexpr uint32_t OFF_RAW = OFF_BIAS + NQ * T::BIAS_TILE;
-  static constexpr uint32_t OFF_DS = OFF_RAW + T::BIAS_TILE;
-  static constexpr uint32_t OFF_LD = OFF_DS + 128 * 128 * 2;  // lse2[128], delta/sqrt(D)[128]
+  static constexpr uint32_t OFF_BIAS = OFF_DO + NQ * T::TILE;      // rows = key k
+  static constexpr uint32_t OFF_RAW = OFF_BIAS + NB * T::BIAS_TILE;
+  static constexpr uint32_t OFF_DS = OFF_RAW + (BIAS_K_CONTIG ? T::BIAS_TILE : 0);
+  static constexpr uint32_t OFF_LD = OFF_DS + 128 * 128 * 2;  // -lse2[128], -delta/sqrt(D)[128]
   static constexpr uint32_t SMEM = OFF_LD + NQ * 256 * 4;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_P = 256, T_DS = 320, T_DQ = 384,
                             T_DK = 384 + 2 * D, T_DV = 384 + 3 * D;
   static_assert(T_DV + D <= 512, "tensor memory overflow");
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory overflow");
   static constexpr int THREADS = 384;
   static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 224;
   static_assert(REGS_LOW * 128 + REGS_HIGH * 256 <= LAUNCH_REGS * THREADS, "register split");
 };
 
 struct DkdvParams {
-  int B, S, H, N, njt, nkt;
+  int B, S, H, N, njt, nkt, n_items;
   const unsigned char* mask;
   int64_t msb, mss, msk;
   const float* lse;
@@ -216,42 +232,54 @@ struct DkdvParams {
   unsigned int* status;
 };
 
+struct DkdvItem {
+  int b, s, h, kt;
+  int64_t row0;  // row of (b, s, h, 0) in a dense [B,S,H,N] array
+};
+
 template <int D, bool BIAS_K_CONTIG>
 __global__ void __launch_bounds__(384, 1)
     k_dkdv(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
            const __grid_constant__ CUtensorMap tm_bias, const DkdvParams p) {
-  using C = DkdvCfg<D>;
+  using C = DkdvCfg<D, BIAS_K_CONTIG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t bar_kv, bar_qd_full[C::NQ], bar_qd_empty[C::NQ], bar_b_full[C::NQ],
-      bar_b_empty[C::NQ], bar_raw, bar_s_full, bar_sdp_free, bar_p_ready, bar_mma_done,
-      bar_dq_free[2], bar_drain;
+  __shared__ uint64_t bar_kv_full[2], bar_kv_empty[2], bar_qd_full[C::NQ], bar_qd_empty[C::NQ],
+      bar_b_full[C::NB], bar_b_empty[C::NB], bar_raw, bar_s_full, bar_sdp_free, bar_p_ready,
+      bar_mma_done, bar_dq_free[2], bar_dkdv_free, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
-  int idx = blockIdx.x;
-  const int kt = idx % p.nkt; idx /= p.nkt;
-  const int h = idx % p.H; idx /= p.H;
-  const int s = idx % p.S;
-  const int b = idx / p.S;
   const int njt = p.njt;
+  const int my_items = (p.n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int total = my_items * njt;  // tiles of this CTA
+  auto item = [&](int n) -> DkdvItem {
+    int idx = (int)blockIdx.x + n * (int)gridDim.x;
+    DkdvItem it;
+    it.kt = idx % p.nkt; idx /= p.nkt;
+    it.h = idx % p.H; idx /= p.H;
+    it.s = idx % p.S;
+    it.b = idx / p.S;
+    it.row0 = (((int64_t)it.b * p.S + it.s) * p.H + it.h) * p.N;
+    return it;
+  };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(&bar_kv, 1);
-    mbar_init(&bar_raw, 1);
-    for (int i = 0; i < C::NQ; ++i) {
-      mbar_init(&bar_qd_full[i], 1); mbar_init(&bar_qd_empty[i], 1);
-      mbar_init(&bar_b_full[i], 1); mbar_init(&bar_b_empty[i], 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_kv_full[i], 1); mbar_init(&bar_kv_empty[i], 1);
+      // one "read" barrier per dQ buffer: a single barrier could complete two
+      // phases (tiles g-2 and g-1) before the MMA thread looks at it
+      mbar_init(&bar_dq_free[i], 256);
     }
+    for (int i = 0; i < C::NQ; ++i) { mbar_init(&bar_qd_full[i], 1); mbar_init(&bar_qd_empty[i], 1); }
+    for (int i = 0; i < C::NB; ++i) { mbar_init(&bar_b_full[i], 1); mbar_init(&bar_b_empty[i], 256); }
+    mbar_init(&bar_raw, 1);
     mbar_init(&bar_s_full, 1); mbar_init(&bar_sdp_free, 256); mbar_init(&bar_p_ready, 256);
-    // one "read" barrier per dQ buffer: a single barrier could complete two
-    // phases (tiles jt-2 and jt-1) before the MMA thread looks at it
-    mbar_init(&bar_mma_done, 1); mbar_init(&bar_dq_free[0], 256); mbar_init(&bar_dq_free[1], 256);
-    mbar_init(&bar_drain, 1);
+    mbar_init(&bar_mma_done, 1); mbar_init(&bar_dkdv_free, 256); mbar_init(&bar_drain, 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(&tmem_slot, 512);
@@ -265,7 +293,6 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = tmem_slot;
   volatile int* abort_p = &abort_flag;
   const WaitCtx wctx{abort_p, p.status};
-  const int64_t row0 = (((int64_t)b * p.S + s) * p.H + h) * p.N;  // row of (b,s,h,0)
   auto teardown = [&]() {
     tc_fence_before();
     __syncthreads();
@@ -284,74 +311,115 @@ __global__ void __launch_bounds__(384, 1)
     // The compute threads read the bias tile by key rows.  A key-row-major
     // tile (queries contiguous: the ending-node view) is fetched straight
     // into its stage; a query-row-major one is staged and transposed.
-    auto issue_bias = [&](int jt, uint8_t* dst, uint64_t* bar) {
+    auto issue_bias = [&](int g, uint8_t* dst, uint64_t* bar) {
+      const DkdvItem it = item(g / njt);
+      const int jt = g % njt;
       mbar_arrive_expect_tx(bar, C::BIAS_TILE);
       if (BIAS_K_CONTIG) {
-        tma_load_4d(dst, &tm_bias, bar, kt * 128, jt * 128, h, b);
-        tma_load_4d(dst + 16384, &tm_bias, bar, kt * 128 + 64, jt * 128, h, b);
+        tma_load_4d(dst, &tm_bias, bar, it.kt * 128, jt * 128, it.h, it.b);
+        tma_load_4d(dst + 16384, &tm_bias, bar, it.kt * 128 + 64, jt * 128, it.h, it.b);
       } else {
-        tma_load_4d(dst, &tm_bias, bar, jt * 128, kt * 128, h, b);
-        tma_load_4d(dst + 16384, &tm_bias, bar, jt * 128 + 64, kt * 128, h, b);
+        tma_load_4d(dst, &tm_bias, bar, jt * 128, it.kt * 128, it.h, it.b);
+        tma_load_4d(dst + 16384, &tm_bias, bar, jt * 128 + 64, it.kt * 128, it.h, it.b);
       }
     };
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bar_kv, 2 * C::TILE);
-      tma_load_5d(smem + C::OFF_K, &tm_k, &bar_kv, 0, kt * 128, h, s, b);
-      tma_load_5d(smem + C::OFF_V, &tm_v, &bar_kv, 0, kt * 128, h, s, b);
-      if (BIAS_K_CONTIG) issue_bias(0, smem + C::OFF_RAW, &bar_raw);
-    }
     const float inv_sqrt_d = rsqrtf((float)D);
     bool ok = true;
-    int issued = 0, raw_issued = BIAS_K_CONTIG ? 1 : 0;
-    for (int jt = 0; jt < njt; ++jt) {
-      const int st = jt % C::NQ;
-      if (jt >= C::NQ) {
-        ok = mbar_wait(&bar_qd_empty[st], ((jt / C::NQ) - 1) & 1, wctx) &&
-             mbar_wait(&bar_b_empty[st], ((jt / C::NQ) - 1) & 1, wctx);
-      }
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      // per-query constants of this tile: lse in log2 units (+inf beyond N
-      // so that P = 0 there) and delta / sqrt(D)
-      float* ld = reinterpret_cast<float*>(smem + C::OFF_LD + st * 1024);
+    int kv_issued = 0, qd_issued = 0, b_issued = 0, raw_issued = 0;
+    if (BIAS_K_CONTIG && total > 0) {
+      if (lane == 0) issue_bias(0, smem + C::OFF_RAW, &bar_raw);
+      raw_issued = 1;
+    }
+    // The per-query constants of tile g+1 are loaded into registers while
+    // tile g is being armed, so the producer never waits on their latency.
+    float pre_l[4], pre_d[4];
+    auto prefetch = [&](int t) {
+      if (t >= total) return;
+      const DkdvItem pt = item(t / njt);
+      const int pjt = t % njt;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int jl = e * 32 + lane, j = jt * 128 + jl;
-        ld[jl] = j < p.N ? p.lse[row0 + j] * kLog2e : INFINITY;
-        ld[128 + jl] = j < p.N ? p.delta[row0 + j] * inv_sqrt_d : 0.f;
+        const int j = pjt * 128 + e * 32 + lane;
+        pre_l[e] = j < p.N ? p.lse[pt.row0 + j] : 0.f;
+        pre_d[e] = j < p.N ? p.delta[pt.row0 + j] : 0.f;
       }
-      __syncwarp();
+    };
+    prefetch(0);
+    int g = 0;
+    for (int n = 0; n < my_items && ok; ++n) {
+      const DkdvItem it = item(n);
+      const int kvs = n & 1;
+      if (n >= 2) ok = mbar_wait(&bar_kv_empty[kvs], ((n >> 1) - 1) & 1, wctx);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bar_qd_full[st], 2 * C::TILE);
-        tma_load_5d(smem + C::OFF_Q + st * C::TILE, &tm_q, &bar_qd_full[st], 0, jt * 128, h, s, b);
-        tma_load_5d(smem + C::OFF_DO + st * C::TILE, &tm_do, &bar_qd_full[st], 0, jt * 128, h, s,
-                    b);
+        mbar_arrive_expect_tx(&bar_kv_full[kvs], 2 * C::TILE);
+        tma_load_5d(smem + C::OFF_K + kvs * C::TILE, &tm_k, &bar_kv_full[kvs], 0, it.kt * 128,
+                    it.h, it.s, it.b);
+        tma_load_5d(smem + C::OFF_V + kvs * C::TILE, &tm_v, &bar_kv_full[kvs], 0, it.kt * 128,
+                    it.h, it.s, it.b);
       }
-      uint8_t* stage = smem + C::OFF_BIAS + st * C::BIAS_TILE;
-      if (!BIAS_K_CONTIG) {
-        if (lane == 0) issue_bias(jt, stage, &bar_b_full[st]);
-      } else {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw, jt & 1, wctx));
+      kv_issued = n + 1;
+      for (int jt = 0; jt < njt; ++jt, ++g) {
+        const int qs = g % C::NQ, bs = g % C::NB;
+        if (g >= C::NQ) ok = mbar_wait(&bar_qd_empty[qs], ((g / C::NQ) - 1) & 1, wctx);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        transpose_tile128_bf16(smem + C::OFF_RAW, stage, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
+        // Q and dOa tiles first; the phase completes only with the arrival
+        // after the per-query constants below
         if (lane == 0) {
-          mbar_arrive(&bar_b_full[st]);
-          if (jt + 1 < njt) issue_bias(jt + 1, smem + C::OFF_RAW, &bar_raw);
+          mbar_expect_tx(&bar_qd_full[qs], 2 * C::TILE);
+          tma_load_5d(smem + C::OFF_Q + qs * C::TILE, &tm_q, &bar_qd_full[qs], 0, jt * 128, it.h,
+                      it.s, it.b);
+          tma_load_5d(smem + C::OFF_DO + qs * C::TILE, &tm_do, &bar_qd_full[qs], 0, jt * 128,
+                      it.h, it.s, it.b);
         }
-        raw_issued = min(jt + 2, njt);
+        // per-query constants of this tile, negated: -lse in log2 units
+        // (-inf beyond N so that P = 0 there) and -delta / sqrt(D)
+        float* ld = reinterpret_cast<float*>(smem + C::OFF_LD + qs * 1024);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int jl = e * 32 + lane, j = jt * 128 + jl;
+          ld[jl] = j < p.N ? -pre_l[e] * kLog2e : -INFINITY;
+          ld[128 + jl] = j < p.N ? -pre_d[e] * inv_sqrt_d : 0.f;
+        }
+        prefetch(g + 1);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_qd_full[qs]);
+        qd_issued = g + 1;
+        if (g >= C::NB) ok = mbar_wait(&bar_b_empty[bs], ((g / C::NB) - 1) & 1, wctx);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        uint8_t* stage = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
+        if (!BIAS_K_CONTIG) {
+          if (lane == 0) issue_bias(g, stage, &bar_b_full[bs]);
+          b_issued = g + 1;
+        } else {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw, g & 1, wctx));
+          if (!ok) break;
+          transpose_tile128_bf16(smem + C::OFF_RAW, stage, lane);
+          fence_proxy_async_smem();  // generic reads of the staging buffer before its next TMA
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bar_b_full[bs]);
+            if (g + 1 < total) issue_bias(g + 1, smem + C::OFF_RAW, &bar_raw);
+          }
+          if (g + 1 < total) raw_issued = g + 2;
+        }
       }
-      issued = jt + 1;
     }
+    // After a give-up, let every copy already issued land before the CTA may
+    // exit (those waits end by themselves: a copy does not depend on the
+    // other roles).
     if (!ok && lane == 0) {
       volatile int no_abort = 0;
-      for (int jt = max(0, issued - C::NQ); jt < issued; ++jt) {
-        mbar_wait(&bar_qd_full[jt % C::NQ], (jt / C::NQ) & 1, &no_abort);
-        if (!BIAS_K_CONTIG) mbar_wait(&bar_b_full[jt % C::NQ], (jt / C::NQ) & 1, &no_abort);
-      }
-      if (BIAS_K_CONTIG && raw_issued > 0) mbar_wait(&bar_raw, (raw_issued - 1) & 1, &no_abort);
-      mbar_wait(&bar_kv, 0, &no_abort);
+      for (int i = max(0, kv_issued - 2); i < kv_issued; ++i)
+        mbar_wait(&bar_kv_full[i & 1], (i >> 1) & 1, &no_abort);
+      for (int i = max(0, qd_issued - C::NQ); i < qd_issued; ++i)
+        mbar_wait(&bar_qd_full[i % C::NQ], (i / C::NQ) & 1, &no_abort);
+      for (int i = max(0, b_issued - C::NB); i < b_issued; ++i)
+        mbar_wait(&bar_b_full[i % C::NB], (i / C::NB) & 1, &no_abort);
+      if (raw_issued > 0) mbar_wait(&bar_raw, (raw_issued - 1) & 1, &no_abort);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -363,53 +431,69 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t sk = smem_u32(smem + C::OFF_K), sv = smem_u32(smem + C::OFF_V),
                      sq = smem_u32(smem + C::OFF_Q), sdo = smem_u32(smem + C::OFF_DO),
                      sds = smem_u32(smem + C::OFF_DS);
-      bool ok = mbar_wait(&bar_kv, 0, wctx);
-      auto issue_sdp = [&](int jt) -> bool {
-        const int st = jt % C::NQ;
-        if (!mbar_wait(&bar_qd_full[st], (jt / C::NQ) & 1, wctx)) return false;
-        tc_fence_after();
+      int a = 0, bq = 0;  // next S/dP tile, next dV/dK/dQ tile
+      Watchdog wd;
+      wd.reset();
+      bool ok = true;
+      while (bq < total) {
+        bool prog = false;
+        if (a < total && a <= bq + 1) {
+          const int n = a / njt, jt = a % njt, qs = a % C::NQ, kvs = n & 1;
+          if ((a == 0 || mbar_test(&bar_sdp_free, (a - 1) & 1)) &&
+              mbar_test(&bar_qd_full[qs], (a / C::NQ) & 1) &&
+              (jt != 0 || mbar_test(&bar_kv_full[kvs], (n >> 1) & 1))) {
+            tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          umma_ss(tmem + C::T_S, umma_desc(sk + kk * 32, 16, C::ATOM, C::SW),
-                  umma_desc(sq + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_sdp, kk > 0);
-          umma_ss(tmem + C::T_DP, umma_desc(sv + kk * 32, 16, C::ATOM, C::SW),
-                  umma_desc(sdo + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_sdp, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              umma_ss(tmem + C::T_S, umma_desc(sk + kvs * C::TILE + kk * 32, 16, C::ATOM, C::SW),
+                      umma_desc(sq + qs * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_sdp, kk > 0);
+              umma_ss(tmem + C::T_DP, umma_desc(sv + kvs * C::TILE + kk * 32, 16, C::ATOM, C::SW),
+                      umma_desc(sdo + qs * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_sdp,
+                      kk > 0);
+            }
+            umma_commit(&bar_s_full);
+            ++a;
+            prog = true;
+          }
         }
-        umma_commit(&bar_s_full);
-        return true;
-      };
-      if (ok) ok = issue_sdp(0);
-      for (int jt = 0; jt < njt && ok; ++jt) {
-        const int st = jt % C::NQ;
-        // S/dP of jt are in registers: the next tile may overwrite them
-        if (jt + 1 < njt) {
-          ok = mbar_wait(&bar_sdp_free, jt & 1, wctx);
-          if (ok) ok = issue_sdp(jt + 1);
-          if (!ok) break;
-        }
-        ok = mbar_wait(&bar_p_ready, jt & 1, wctx);
-        // the dQ buffer of this tile was last read for tile jt-2
-        if (ok && jt >= 2) ok = mbar_wait(&bar_dq_free[jt & 1], ((jt >> 1) - 1) & 1, wctx);
-        if (!ok) break;
-        tc_fence_after();
+        if (bq < a) {
+          const int n = bq / njt, jt = bq % njt, qs = bq % C::NQ, kvs = n & 1;
+          if (mbar_test(&bar_p_ready, bq & 1) &&
+              (bq < 2 || mbar_test(&bar_dq_free[bq & 1], ((bq >> 1) - 1) & 1)) &&
+              (jt != 0 || n == 0 || mbar_test(&bar_dkdv_free, (n - 1) & 1))) {
+            tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t acc = (jt > 0 || kk > 0) ? 1u : 0u;
-          // dV += P^T dOa ; dK += dS^T Q  (K dimension = queries, 16 per step)
-          umma_ts(tmem + C::T_DV, tmem + C::T_P + kk * 8,
-                  umma_desc(sdo + st * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_kv,
-                  acc);
-          umma_ts(tmem + C::T_DK, tmem + C::T_DS + kk * 8,
-                  umma_desc(sq + st * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_kv,
-                  acc);
-        }
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t acc = (jt > 0 || kk > 0) ? 1u : 0u;
+              // dV += P^T dOa ; dK += dS^T Q  (K dimension = queries, 16 per step)
+              umma_ts(tmem + C::T_DV, tmem + C::T_P + kk * 8,
+                      umma_desc(sdo + qs * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_kv,
+                      acc);
+              umma_ts(tmem + C::T_DK, tmem + C::T_DS + kk * 8,
+                      umma_desc(sq + qs * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_kv,
+                      acc);
+            }
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K dimension = keys)
-          umma_ss(tmem + C::T_DQ + (jt & 1) * D, umma_desc(sds + kk * 2048, 16384, 1024, kSw128),
-                  umma_desc(sk + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_q, kk > 0);
-        umma_commit(&bar_qd_empty[st]);
-        umma_commit(&bar_mma_done);
+            for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K dimension = keys)
+              umma_ss(tmem + C::T_DQ + (bq & 1) * D,
+                      umma_desc(sds + kk * 2048, 16384, 1024, kSw128),
+                      umma_desc(sk + kvs * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_q,
+                      kk > 0);
+            umma_commit(&bar_qd_empty[qs]);
+            if (jt == njt - 1) umma_commit(&bar_kv_empty[kvs]);
+            umma_commit(&bar_mma_done);
+            ++bq;
+            prog = true;
+          }
+        }
+        if (prog) {
+          wd.reset();
+        } else if (!wd.poll(wctx)) {
+          ok = false;
+          break;
+        }
       }
+      (void)ok;
       umma_commit(&bar_drain);
       volatile int no_abort = 0;
       mbar_wait(&bar_drain, 0, &no_abort);
@@ -424,19 +508,14 @@ __global__ void __launch_bounds__(384, 1)
     const int wg = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int kl = quad * 32 + lane;          // key within the tile (TMEM lane)
-    const int kg = kt * 128 + kl;             // key index
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const float c1 = kLog2e * rsqrtf((float)D);
     const float inv_sqrt_d = rsqrtf((float)D);
-    // additive mask of this key, log2 units (constant over the query tiles)
-    float madd = 0.f;
-    if (kg >= p.N) madd = -INFINITY;
-    else if (p.mask && !p.mask[b * p.msb + (int64_t)s * p.mss + (int64_t)kg * p.msk])
-      madd = kMaskBias * kLog2e;
     const float2 c1c1 = make_float2(c1, c1), l2l2 = make_float2(kLog2e, kLog2e),
-                 mm = make_float2(madd, madd), isd = make_float2(inv_sqrt_d, inv_sqrt_d);
-    // dQ partial of tile t: lane = query; this warpgroup adds half of D
-    auto dq_epilogue = [&](int t) {
+                 isd = make_float2(inv_sqrt_d, inv_sqrt_d);
+    // dQ partial of tile t (query tile jt_t of the item at row0_t): lane =
+    // query; this warpgroup adds half of D
+    auto dq_epilogue = [&](int t, int64_t row0_t, int jt_t) {
       uint32_t q16[D / 2];
       if constexpr (D == 32) {
         tmem_ld16(lane_base + C::T_DQ + (t & 1) * D + 16 * wg,
@@ -450,9 +529,9 @@ __global__ void __launch_bounds__(384, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&bar_dq_free[t & 1]);
-      const int jg = t * 128 + kl;  // this lane's query row
+      const int jg = jt_t * 128 + kl;  // this lane's query row
       if (jg < p.N) {
-        float* dst = p.dq_acc + (row0 + jg) * D + (D / 2) * wg;
+        float* dst = p.dq_acc + (row0_t + jg) * D + (D / 2) * wg;
 #pragma unroll
         for (int e = 0; e < D / 2; e += 4)
           red_add_v4(dst + e, __uint_as_float(q16[e]), __uint_as_float(q16[e + 1]),
@@ -460,96 +539,106 @@ __global__ void __launch_bounds__(384, 1)
       }
     };
     bool ok = true;
-    for (int jt = 0; jt < njt; ++jt) {
-      const int st = jt % C::NQ;
-      ok = mbar_wait(&bar_s_full, jt & 1, wctx) &&
-           mbar_wait(&bar_qd_full[st], (jt / C::NQ) & 1, wctx) &&
-           mbar_wait(&bar_b_full[st], (jt / C::NQ) & 1, wctx);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sx[64], dpx[64];
-      tmem_ld32(lane_base + C::T_S + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&sx[0]));
-      tmem_ld32(lane_base + C::T_S + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&sx[32]));
-      tmem_ld32(lane_base + C::T_DP + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&dpx[0]));
-      tmem_ld32(lane_base + C::T_DP + 64 * wg + 32,
-                *reinterpret_cast<uint32_t(*)[32]>(&dpx[32]));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bar_sdp_free);
-      const float* ld = reinterpret_cast<const float*>(smem + C::OFF_LD + st * 1024);
-      // bias row of this key, this warpgroup's 64 queries (one 64-wide box)
-      const uint8_t* brow = smem + C::OFF_BIAS + st * C::BIAS_TILE + wg * 16384 + kl * 128;
-      uint32_t pk[32], dk2[32];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {  // 8 queries per step
-        const uint4 w4 = *reinterpret_cast<const uint4*>(brow + ((c ^ (kl & 7)) << 4));
-        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-        const float4 la = *reinterpret_cast<const float4*>(ld + 64 * wg + 8 * c);
-        const float4 lb = *reinterpret_cast<const float4*>(ld + 64 * wg + 8 * c + 4);
-        const float4 da = *reinterpret_cast<const float4*>(ld + 128 + 64 * wg + 8 * c);
-        const float4 db = *reinterpret_cast<const float4*>(ld + 128 + 64 * wg + 8 * c + 4);
-        const float2 nl[4] = {make_float2(-la.x, -la.y), make_float2(-la.z, -la.w),
-                              make_float2(-lb.x, -lb.y), make_float2(-lb.z, -lb.w)};
-        const float2 nd[4] = {make_float2(-da.x, -da.y), make_float2(-da.z, -da.w),
-                              make_float2(-db.x, -db.y), make_float2(-db.z, -db.w)};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j2 = 8 * c + 2 * e;
-          float2 t = fma2(make_float2(__uint_as_float(sx[j2]), __uint_as_float(sx[j2 + 1])),
-                          c1c1, mm);
-          t = fma2(make_float2(bf16lo(wv[e]), bf16hi(wv[e])), l2l2, t);
-          t = add2(t, nl[e]);
-          const float2 pr = make_float2(ex2(t.x), ex2(t.y));
-          const float2 g = fma2(make_float2(__uint_as_float(dpx[j2]), __uint_as_float(dpx[j2 + 1])),
-                                isd, nd[e]);
-          const float2 ds = mul2(pr, g);
-          pk[4 * c + e] = pack_bf16(pr.x, pr.y);
-          dk2[4 * c + e] = pack_bf16(ds.x, ds.y);
-        }
-      }
-      mbar_arrive(&bar_b_empty[st]);
-      // the previous tile's MMAs read P^T, dS^T and the dS tile: wait for them
-      if (jt > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done, (jt - 1) & 1, wctx));
+    int g = 0;
+    for (int n = 0; n < my_items && ok; ++n) {
+      const DkdvItem it = item(n);
+      const int kg = it.kt * 128 + kl;  // key index
+      // additive mask of this key, log2 units (constant over the query tiles)
+      float madd = 0.f;
+      if (kg >= p.N) madd = -INFINITY;
+      else if (p.mask && !p.mask[it.b * p.msb + (int64_t)it.s * p.mss + (int64_t)kg * p.msk])
+        madd = kMaskBias * kLog2e;
+      const float2 mm = make_float2(madd, madd);
+      for (int jt = 0; jt < njt; ++jt, ++g) {
+        const int qs = g % C::NQ, bs = g % C::NB;
+        ok = mbar_wait(&bar_s_full, g & 1, wctx) &&
+             mbar_wait(&bar_qd_full[qs], (g / C::NQ) & 1, wctx) &&
+             mbar_wait(&bar_b_full[bs], (g / C::NB) & 1, wctx);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-      }
-      tmem_st32(lane_base + C::T_P + 32 * wg, pk);
-      tmem_st32(lane_base + C::T_DS + 32 * wg, dk2);
-      // dS into shared memory as the M-major A operand of dQ = dS K: row k,
-      // queries of this half contiguous, 128-byte swizzle.
-      {
-        uint8_t* rowp = smem + C::OFF_DS + wg * 16384 + (kl >> 3) * 1024 + (kl & 7) * 128;
+        uint32_t sx[64], dpx[64];
+        tmem_ld32(lane_base + C::T_S + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&sx[0]));
+        tmem_ld32(lane_base + C::T_S + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&sx[32]));
+        tmem_ld32(lane_base + C::T_DP + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&dpx[0]));
+        tmem_ld32(lane_base + C::T_DP + 64 * wg + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(&dpx[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bar_sdp_free);
+        const float* ld = reinterpret_cast<const float*>(smem + C::OFF_LD + qs * 1024);
+        // bias row of this key, this warpgroup's 64 queries (one 64-wide box)
+        const uint8_t* brow = smem + C::OFF_BIAS + bs * C::BIAS_TILE + wg * 16384 + kl * 128;
+        uint32_t pk[32], dk2[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(rowp + ((c ^ (kl & 7)) << 4)) =
-              make_uint4(dk2[4 * c], dk2[4 * c + 1], dk2[4 * c + 2], dk2[4 * c + 3]);
+        for (int c = 0; c < 8; ++c) {  // 8 queries per step
+          const uint4 w4 = *reinterpret_cast<const uint4*>(brow + ((c ^ (kl & 7)) << 4));
+          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+          const float4 la = *reinterpret_cast<const float4*>(ld + 64 * wg + 8 * c);
+          const float4 lb = *reinterpret_cast<const float4*>(ld + 64 * wg + 8 * c + 4);
+          const float4 da = *reinterpret_cast<const float4*>(ld + 128 + 64 * wg + 8 * c);
+          const float4 db = *reinterpret_cast<const float4*>(ld + 128 + 64 * wg + 8 * c + 4);
+          const float2 nl[4] = {make_float2(la.x, la.y), make_float2(la.z, la.w),
+                                make_float2(lb.x, lb.y), make_float2(lb.z, lb.w)};
+          const float2 nd[4] = {make_float2(da.x, da.y), make_float2(da.z, da.w),
+                                make_float2(db.x, db.y), make_float2(db.z, db.w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j2 = 8 * c + 2 * e;
+            float2 t = fma2(make_float2(__uint_as_float(sx[j2]), __uint_as_float(sx[j2 + 1])),
+                            c1c1, mm);
+            t = fma2(make_float2(bf16lo(wv[e]), bf16hi(wv[e])), l2l2, t);
+            t = add2(t, nl[e]);
+            const float2 pr = make_float2(ex2(t.x), ex2(t.y));
+            const float2 gg = fma2(
+                make_float2(__uint_as_float(dpx[j2]), __uint_as_float(dpx[j2 + 1])), isd, nd[e]);
+            const float2 ds = mul2(pr, gg);
+            pk[4 * c + e] = pack_bf16(pr.x, pr.y);
+            dk2[4 * c + e] = pack_bf16(ds.x, ds.y);
+          }
+        }
+        mbar_arrive(&bar_b_empty[bs]);
+        // the previous tile's MMAs read P^T, dS^T and the dS tile: wait for them
+        if (g > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done, (g - 1) & 1, wctx));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        tmem_st32(lane_base + C::T_P + 32 * wg, pk);
+        tmem_st32(lane_base + C::T_DS + 32 * wg, dk2);
+        // dS into shared memory as the M-major A operand of dQ = dS K: row k,
+        // queries of this half contiguous, 128-byte swizzle.
+        {
+          uint8_t* rowp = smem + C::OFF_DS + wg * 16384 + (kl >> 3) * 1024 + (kl & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(rowp + ((c ^ (kl & 7)) << 4)) =
+                make_uint4(dk2[4 * c], dk2[4 * c + 1], dk2[4 * c + 2], dk2[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_p_ready);
+        if (jt > 0) dq_epilogue(g - 1, it.row0, jt - 1);  // its MMAs completed (waited above)
       }
-      fence_proxy_async_smem();
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar_p_ready);
-      if (jt > 0) dq_epilogue(jt - 1);   // its MMAs completed (waited above)
-    }
-    if (ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done, (njt - 1) & 1, wctx));
-      if (ok) {
-        tc_fence_after();
-        dq_epilogue(njt - 1);
-      }
-    }
-    // ---- dK (warpgroup 0) and dV (warpgroup 1) of this key tile -----------
-    if (ok) {
+      if (!ok) break;
+      // ---- end of the item: last dQ partial, then dK (warpgroup 0) and dV
+      // (warpgroup 1) of this key tile ---------------------------------------
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done, (g - 1) & 1, wctx));
+      if (!ok) break;
+      tc_fence_after();
+      dq_epilogue(g - 1, it.row0, njt - 1);
       uint32_t r[D];
       const uint32_t col = wg == 0 ? C::T_DK : C::T_DV;
 #pragma unroll
       for (int c = 0; c < D / 16; ++c)
         tmem_ld16(lane_base + col + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * c]));
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bar_dkdv_free);
       if (kg < p.N) {
-        __nv_bfloat16* dst =
-            wg == 0 ? p.dk + p.sdk.at(b, s, h, kg, 0) : p.dv + p.sdv.at(b, s, h, kg, 0);
+        __nv_bfloat16* dst = wg == 0 ? p.dk + p.sdk.at(it.b, it.s, it.h, kg, 0)
+                                     : p.dv + p.sdv.at(it.b, it.s, it.h, kg, 0);
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
           float f[8];
@@ -962,9 +1051,12 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
   if (ev) cudaEventRecord(ev[1], st);
   // 2) dK, dV (+ dQ partial sums)
   {
-    using C = DkdvCfg<D>;
+    using C = DkdvCfg<D, KC>;
     DkdvParams dp{};
     dp.B = P.B; dp.S = P.S; dp.H = P.H; dp.N = P.N; dp.njt = nt; dp.nkt = nt;
+    const int64_t items = (int64_t)P.B * P.S * P.H * nt;
+    if (items > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    dp.n_items = (int)items;
     dp.mask = a.mask; dp.msb = P.mask.b; dp.mss = P.mask.s; dp.msk = P.mask.k;
     dp.lse = a.lse; dp.delta = w.delta; dp.dq_acc = w.dq_acc;
     dp.dk = static_cast<__nv_bfloat16*>(a.dk); dp.dv = static_cast<__nv_bfloat16*>(a.dv);
@@ -974,9 +1066,13 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     if (e != cudaSuccess) return e;
     e = check_regs(kern, C::LAUNCH_REGS);
     if (e != cudaSuccess) return e;
-    const uint64_t grid = (uint64_t)P.B * P.S * P.H * nt;
-    if (grid > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, tb, dp);
+    // persistent: one CTA per SM (each holds 512 TMEM columns)
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)std::min<int64_t>(items, (int64_t)std::max(sms, 1));
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, tb, dp);
   }
   if (ev) cudaEventRecord(ev[2], st);
   // 3) dbias partials

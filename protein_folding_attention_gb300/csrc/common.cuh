@@ -62,6 +62,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// Raise the expected transaction count of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -70,6 +75,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       " selp.b32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of a phase (for issuers that poll several barriers).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.b32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -111,6 +129,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
   }
 }
+
+// Progress watchdog for a polling loop: call poll() after each round that
+// made no progress; it returns false once the loop has been stuck for the
+// wait limit or another thread/CTA gave up (and reports like mbar_wait).
+struct Watchdog {
+  unsigned long long t0;
+  uint32_t n;
+  __device__ __forceinline__ void reset() { t0 = globaltimer_ns(); n = 0; }
+  __device__ __forceinline__ bool poll(const WaitCtx& w) {
+    if (*w.abort_flag) return false;
+    if ((++n & 63) == 0) {
+      if (w.status && (*w.status & (1u << EVOATTN_ERR_TIMEOUT))) {
+        *w.abort_flag = 1;
+        return false;
+      }
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        *w.abort_flag = 1;
+        if (w.status) atomicOr(const_cast<unsigned int*>(w.status), 1u << EVOATTN_ERR_TIMEOUT);
+        return false;
+      }
+    }
+    return true;
+  }
+};
 
 // Bounded wait used while winding down after a give-up (for copies and MMAs
 // already issued, which complete by themselves): no early exit.
