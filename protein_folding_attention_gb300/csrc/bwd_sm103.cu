@@ -658,9 +658,10 @@ __global__ void __launch_bounds__(384, 1)
 // CTA = (b, h, query tile jt, key tile kt, s-slot).  Warps (384 threads): 0
 // producer, 1 MMA, 2-3 idle, 4-11 two compute warpgroups; a compute thread
 // owns query j (TMEM lane) and the 64 keys of its warpgroup's half.  Tensor
-// memory: S 0..127, dP 128..255, dbias accumulator 256..383 (fp32, lane =
-// query).  The bias tile is fetched once per CTA with query rows (transposed
-// in shared memory when the view has queries contiguous).
+// memory: S 0..127, dP 128..255 (fp32, lane =
+// query); each compute thread keeps its 64 dbias sums in registers across
+// the slot's s.  The bias tile is fetched once per CTA with query rows
+// (transposed in shared memory when the view has queries contiguous).
 template <int D>
 struct DbiasCfg : Tile<D> {
   using T = Tile<D>;
@@ -674,7 +675,7 @@ struct DbiasCfg : Tile<D> {
   static constexpr uint32_t OFF_MADD = OFF_RAW + T::BIAS_TILE;
   static constexpr uint32_t SMEM = OFF_MADD + NST * 128 * 4;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
-  static constexpr uint32_t T_S = 0, T_DP = 128, T_ACC = 256;
+  static constexpr uint32_t T_S = 0, T_DP = 128;
   static constexpr int THREADS = 384;
   static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 224;
   static_assert(REGS_LOW * 128 + REGS_HIGH * 256 <= LAUNCH_REGS * THREADS, "register split");
@@ -767,21 +768,33 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
     int issued = 0;
+    // mask bytes of the next s are loaded while the current one is armed
+    unsigned char pre_m[4];
+    auto prefetch_mask = [&](int i) {
+      if (i >= ns || !p.mask) return;
+      const unsigned char* mrow = p.mask + b * p.msb + (int64_t)(s_begin + i) * p.mss;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int kk = kt * 128 + e * 32 + lane;
+        pre_m[e] = kk < p.N ? mrow[kk * p.msk] : 0;
+      }
+    };
+    prefetch_mask(0);
     for (int i = 0; i < ns; ++i) {
       const int st = i % C::NST, s = s_begin + i;
       if (i >= C::NST) ok = mbar_wait(&bar_empty[st], ((i / C::NST) - 1) & 1, wctx);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       float* madd = reinterpret_cast<float*>(smem + C::OFF_MADD + st * 512);
-      const unsigned char* mrow = p.mask ? p.mask + b * p.msb + (int64_t)s * p.mss : nullptr;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int kk = kt * 128 + e * 32 + lane;
         float a = 0.f;
         if (kk >= p.N) a = -INFINITY;
-        else if (mrow && !mrow[kk * p.msk]) a = kMaskBias * kLog2e;
+        else if (p.mask && !pre_m[e]) a = kMaskBias * kLog2e;
         madd[e * 32 + lane] = a;
       }
+      prefetch_mask(i + 1);
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar_full[st], 4 * C::TILE);
@@ -851,23 +864,34 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_bias, 0, wctx));
     // this query's 64 bias values (one 64-wide box), query-row layout
     const uint8_t* brow = smem + C::OFF_BIAS + wg * 16384 + jl * 128;
+    // dbias accumulators of this thread's 64 keys, in registers across all s
+    float2 acc[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = make_float2(0.f, 0.f);
+    // lse and delta of the next s are loaded while the current one computes
+    float pre_l = 0.f, pre_d = 0.f;
+    auto prefetch = [&](int i) {
+      if (i >= ns || jg >= p.N) return;
+      const int64_t row = (((int64_t)b * p.S + s_begin + i) * p.H + h) * p.N + jg;
+      pre_l = p.lse[row];
+      pre_d = p.delta[row];
+    };
+    prefetch(0);
     for (int i = 0; i < ns && ok; ++i) {
-      const int st = i % C::NST, s = s_begin + i;
+      const int st = i % C::NST;
+      const float nlse2 = jg < p.N ? -pre_l * kLog2e : -INFINITY;
+      const float ndl = jg < p.N ? -pre_d : 0.f;
+      prefetch(i + 1);
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, i & 1, wctx));
       if (!ok) break;
       tc_fence_after();
-      const int64_t row = (((int64_t)b * p.S + s) * p.H + h) * p.N + jg;
-      const float lse2 = jg < p.N ? p.lse[row] * kLog2e : INFINITY;
-      const float dl = jg < p.N ? p.delta[row] : 0.f;
-      const float2 nl = make_float2(-lse2, -lse2), nd = make_float2(-dl, -dl);
+      const float2 nl = make_float2(nlse2, nlse2), nd = make_float2(ndl, ndl);
       const float* madd = reinterpret_cast<const float*>(smem + C::OFF_MADD + st * 512);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t sx[32], dpx[32], a[32];
-        const uint32_t col = C::T_ACC + 64 * wg + 32 * half;
+        uint32_t sx[32], dpx[32];
         tmem_ld32(lane_base + C::T_S + 64 * wg + 32 * half, sx);
         tmem_ld32(lane_base + C::T_DP + 64 * wg + 32 * half, dpx);
-        if (i > 0) tmem_ld32(lane_base + col, a);
         tmem_wait_ld();
         if (half == 1) {  // S and dP of this s are in registers
           tc_fence_before();
@@ -890,49 +914,42 @@ __global__ void __launch_bounds__(384, 1)
             t = fma2(make_float2(bf16lo(wv[e]), bf16hi(wv[e])), l2l2, t);
             t = add2(t, nl);
             const float2 pr = make_float2(ex2(t.x), ex2(t.y));
-            const float2 g =
+            const float2 gg =
                 add2(make_float2(__uint_as_float(dpx[k2]), __uint_as_float(dpx[k2 + 1])), nd);
-            float2 ds = mul2(pr, g);
-            if (i > 0) ds = add2(ds, make_float2(__uint_as_float(a[k2]), __uint_as_float(a[k2 + 1])));
-            a[k2] = __float_as_uint(ds.x);
-            a[k2 + 1] = __float_as_uint(ds.y);
+            acc[16 * half + 4 * c + e] = fma2(pr, gg, acc[16 * half + 4 * c + e]);
           }
         }
-        tmem_st32(lane_base + col, a);
       }
-      tmem_wait_st();
       mbar_arrive(&bar_empty[st]);
     }
     // ---- write this slot's partial (or add it atomically) ------------------
-    if (ok && ns > 0) {
-      tc_fence_after();
+    if (ok && ns > 0 && jg < p.N) {
+      const int64_t base = ((int64_t)b * p.H + h) * p.N * p.N + (int64_t)jg * p.N;
+      float* dst = p.atomic ? p.out + base : p.out + (int64_t)slot * p.B * p.H * p.N * p.N + base;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t a[32];
-        tmem_ld32(lane_base + C::T_ACC + 64 * wg + 32 * half, a);
-        tmem_wait_ld();
         const int k0 = kt * 128 + 64 * wg + 32 * half;
-        if (jg < p.N) {
-          const int64_t base = ((int64_t)b * p.H + h) * p.N * p.N + (int64_t)jg * p.N;
-          float* dst = p.atomic ? p.out + base
-                                : p.out + (int64_t)slot * p.B * p.H * p.N * p.N + base;
-          if (k0 + 32 <= p.N && (p.N & 3) == 0) {
+        const float2* a2 = acc + 16 * half;
+        if (k0 + 32 <= p.N && (p.N & 3) == 0) {
 #pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              if (p.atomic)
-                red_add_v4(dst + k0 + c, __uint_as_float(a[c]), __uint_as_float(a[c + 1]),
-                           __uint_as_float(a[c + 2]), __uint_as_float(a[c + 3]));
-              else
-                *reinterpret_cast<float4*>(dst + k0 + c) =
-                    make_float4(__uint_as_float(a[c]), __uint_as_float(a[c + 1]),
-                                __uint_as_float(a[c + 2]), __uint_as_float(a[c + 3]));
+          for (int c = 0; c < 16; c += 2) {
+            if (p.atomic)
+              red_add_v4(dst + k0 + 2 * c, a2[c].x, a2[c].y, a2[c + 1].x, a2[c + 1].y);
+            else
+              *reinterpret_cast<float4*>(dst + k0 + 2 * c) =
+                  make_float4(a2[c].x, a2[c].y, a2[c + 1].x, a2[c + 1].y);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            if (k0 + 2 * c < p.N) {
+              if (p.atomic) atomicAdd(dst + k0 + 2 * c, a2[c].x);
+              else dst[k0 + 2 * c] = a2[c].x;
             }
-          } else {
-            for (int c = 0; c < 32; ++c)
-              if (k0 + c < p.N) {
-                if (p.atomic) atomicAdd(dst + k0 + c, __uint_as_float(a[c]));
-                else dst[k0 + c] = __uint_as_float(a[c]);
-              }
+            if (k0 + 2 * c + 1 < p.N) {
+              if (p.atomic) atomicAdd(dst + k0 + 2 * c + 1, a2[c].y);
+              else dst[k0 + 2 * c + 1] = a2[c].y;
+            }
           }
         }
       }

@@ -16,7 +16,7 @@
 //               each (kt, s) and the additive key mask of that (s, kt)
 //   warp 1      MMA issuer (one thread): S = Q K^T into TMEM, O += P V with
 //               P read from TMEM
-//   warps 2-3   idle
+//   warps 2-3   idle (their warpgroup hands registers to the softmax)
 //   warps 4-7   softmax warpgroup 0: rows s = 0, 2, ... of the group
 //   warps 8-11  softmax warpgroup 1: rows s = 1, 3, ...
 // A softmax thread owns one query row j (TMEM lane 32*(warp%4) + lane).
@@ -65,6 +65,10 @@ struct FwdCfg {
   static constexpr uint32_t TMEM_P = 256;
   static constexpr uint32_t TMEM_O = 384;
   static constexpr int THREADS = 384;
+  // register split: launch 168/thread; the producer warpgroup drops to 80,
+  // the softmax warpgroups rise to 208 (80*128 + 208*256 <= 168*384)
+  static constexpr int LAUNCH_REGS = 168, REGS_LOW = 80, REGS_HIGH = 208;
+  static_assert(REGS_LOW * 128 + REGS_HIGH * 256 <= LAUNCH_REGS * THREADS, "register split");
   static_assert(TMEM_O + G * D <= TMEM_COLS, "tensor memory overflow");
 };
 
@@ -153,6 +157,8 @@ __global__ void __launch_bounds__(384, 1)
   };
 
   if (warp < 4) {
+  // setmaxnreg is warpgroup-aligned: one instance for warps 0-3, one for 4-11
+  regs_dec<C::REGS_LOW>();
   if (warp == 0) {
     // =================== TMA producer (whole warp) ========================
     // A query-row-major bias tile ([j][k], keys contiguous) goes straight to
@@ -176,6 +182,19 @@ __global__ void __launch_bounds__(384, 1)
     }
     bool ok = true;
     int kv_issued = 0, bias_issued = 0, raw_issued = BIAS_K_CONTIG ? 0 : 1;
+    // mask bytes of the next (kt, s) are loaded while the current is armed
+    unsigned char pre_m[4];
+    auto prefetch_mask = [&](int i) {
+      if (i >= total || !p.mask) return;
+      const int pkt = i / g_eff, ps = i % g_eff;
+      const unsigned char* mrow = p.mask + b * p.msb + (int64_t)(s0 + ps) * p.mss;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int kk = pkt * C::BN + e * 32 + lane;
+        pre_m[e] = kk < p.N ? mrow[kk * p.msk] : 0;
+      }
+    };
+    prefetch_mask(0);
     for (int kt = 0; kt < nkt && ok; ++kt) {
       const int bs = kt & 1;
       uint8_t* stage = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
@@ -206,16 +225,15 @@ __global__ void __launch_bounds__(384, 1)
         // additive key mask of (s, kt) in log2 units: 0 kept, -1e9*log2(e)
         // masked, -inf beyond N
         float* madd = reinterpret_cast<float*>(smem + C::OFF_MADD + st * C::BN * 4);
-        const unsigned char* mrow =
-            p.mask ? p.mask + b * p.msb + (int64_t)(s0 + s) * p.mss : nullptr;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int kk = kt * C::BN + e * 32 + lane;
           float a = 0.f;
           if (kk >= p.N) a = -INFINITY;
-          else if (mrow && !mrow[kk * p.msk]) a = kMaskBias * kLog2e;
+          else if (p.mask && !pre_m[e]) a = kMaskBias * kLog2e;
           madd[e * 32 + lane] = a;
         }
+        prefetch_mask(i + 1);
         __syncwarp();
         if (lane == 0) {
           mbar_arrive_expect_tx(&bar_kv_full[st], 2 * C::TILE);
@@ -251,49 +269,50 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t sq = smem_u32(smem + C::OFF_Q), sk = smem_u32(smem + C::OFF_K),
                      sv = smem_u32(smem + C::OFF_V);
       bool ok = mbar_wait(&bar_q, 0, wctx);
-      auto issue_qk = [&](int i) -> bool {
-        const int s = i % g_eff, st = i % C::NS, w = s & 1;
-        if (!mbar_wait(&bar_kv_full[st], (i / C::NS) & 1, wctx)) return false;
-        tc_fence_after();
+      // Poll: issue S = QK^T of tile a as soon as its K/V stage is loaded and
+      // its warpgroup has taken its previous S into registers, and O += PV of
+      // tile bq as soon as its P is stored, so neither warpgroup waits for
+      // the other.
+      int a = 0, bq = 0;
+      int n_qk[2] = {0, 0}, n_pv[2] = {0, 0};  // per-warpgroup counts issued
+      Watchdog wd;
+      wd.reset();
+      while (ok && bq < total) {
+        bool prog = false;
+        if (a < total) {
+          const int s = a % g_eff, st = a % C::NS, w = s & 1;
+          if ((n_qk[w] == 0 || mbar_test(&bar_s_free[w], (n_qk[w] - 1) & 1)) &&
+              mbar_test(&bar_kv_full[st], (a / C::NS) & 1)) {
+            tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + 128 * w, umma_desc(sq + s * C::TILE + kk * 32, 16, C::ATOM, C::SW),
-                  umma_desc(sk + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_s, kk > 0);
-        umma_commit(&bar_s_full[w]);
-        return true;
-      };
-      // the iteration after i done by the same warpgroup (rows s of equal parity)
-      auto next_same = [&](int i) -> int {
-        for (int j = i + 1; j < total; ++j)
-          if (((j % g_eff) & 1) == ((i % g_eff) & 1)) return j;
-        return -1;
-      };
-      int wg_iter[2] = {0, 0};
-      if (ok) ok = issue_qk(0);
-      if (ok && g_eff >= 2) ok = issue_qk(1);
-      for (int i = 0; i < total && ok; ++i) {
-        const int kt = i / g_eff, s = i % g_eff, st = i % C::NS, w = s & 1;
-        const uint32_t par = wg_iter[w] & 1;
-        ++wg_iter[w];
-        // the next S of this warpgroup goes to TMEM after this PV (issuing it
-        // earlier would make this single thread block on one warpgroup while
-        // the other one waits for its PV)
-        const int nxt = next_same(i);
-        ok = mbar_wait(&bar_p_ready[w], par, wctx);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::TMEM_O + s * D, tmem + C::TMEM_P + 64 * w + kk * 8,
-                  umma_desc(sv + st * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_o,
-                  (kt > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bar_kv_empty[st]);
-        umma_commit(&bar_o_done[s]);
-        umma_commit(&bar_p_free[w]);
-        if (nxt >= 0) {
-          ok = mbar_wait(&bar_s_free[w], par, wctx);
-          if (ok) ok = issue_qk(nxt);
+            for (int kk = 0; kk < D / 16; ++kk)
+              umma_ss(tmem + 128 * w, umma_desc(sq + s * C::TILE + kk * 32, 16, C::ATOM, C::SW),
+                      umma_desc(sk + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_s, kk > 0);
+            umma_commit(&bar_s_full[w]);
+            ++n_qk[w];
+            ++a;
+            prog = true;
+          }
         }
+        if (bq < a) {
+          const int kt = bq / g_eff, s = bq % g_eff, st = bq % C::NS, w = s & 1;
+          if (mbar_test(&bar_p_ready[w], n_pv[w] & 1)) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ts(tmem + C::TMEM_O + s * D, tmem + C::TMEM_P + 64 * w + kk * 8,
+                      umma_desc(sv + st * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_o,
+                      (kt > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&bar_kv_empty[st]);
+            umma_commit(&bar_o_done[s]);
+            umma_commit(&bar_p_free[w]);
+            ++n_pv[w];
+            ++bq;
+            prog = true;
+          }
+        }
+        if (prog) wd.reset();
+        else if (!wd.poll(wctx)) ok = false;
       }
       // every issued MMA completes before TMEM can be released
       umma_commit(&bar_drain);
@@ -306,6 +325,7 @@ __global__ void __launch_bounds__(384, 1)
   teardown();
   } else {
     // =================== softmax warpgroups ================================
+    regs_inc<C::REGS_HIGH>();
     const int wg = (warp - 4) >> 2;                  // 0 or 1
     const int quad = warp & 3;                       // TMEM lane quadrant
     const int row = quad * 32 + lane;                // query row within the tile
@@ -504,6 +524,12 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
+  // The warpgroups' register split must fit the pool the CTA is launched
+  // with, or the raising warpgroups would wait forever.
+  cudaFuncAttributes fa{};
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(q, k, v, bias, fp);
   return cudaGetLastError();
 }
