@@ -371,12 +371,15 @@ __device__ __forceinline__ uint32_t swz128_chunk(uint32_t base, int r, int c8) {
   return base + (uint32_t)((c8 >> 3) * 16384 + r * 128 + (((c8 & 7) ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ void transpose_tile128_bf16(const void* src, void* dst, int lane) {
+// Blocks [blk_begin, blk_begin + nblk) of the 256 8x8 blocks (nblk a
+// multiple of 4; several warps can split a tile).
+__device__ __forceinline__ void transpose_tile128_bf16(const void* src, void* dst, int lane,
+                                                       int blk_begin = 0, int nblk = 256) {
   const uint32_t s = smem_u32(src), d = smem_u32(dst);
   const int m = lane >> 3, i = lane & 7;  // matrix of this lane's address, row within it
 #pragma unroll 4
-  for (int it = 0; it < 64; ++it) {
-    const int blk = it * 4 + m;            // 256 8x8 blocks
+  for (int it = 0; it < nblk / 4; ++it) {
+    const int blk = blk_begin + it * 4 + m;
     const int rb = blk >> 4, cb = blk & 15;
     uint32_t r0, r1, r2, r3;
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"

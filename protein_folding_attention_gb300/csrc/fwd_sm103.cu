@@ -16,7 +16,8 @@
 //               each (kt, s) and the additive key mask of that (s, kt)
 //   warp 1      MMA issuer (one thread): S = Q K^T into TMEM, O += P V with
 //               P read from TMEM
-//   warps 2-3   idle (their warpgroup hands registers to the softmax)
+//   warps 2-3   transpose a key-row-major (query-contiguous) bias tile into
+//               query rows; idle otherwise
 //   warps 4-7   softmax warpgroup 0: rows s = 0, 2, ... of the group
 //   warps 8-11  softmax warpgroup 1: rows s = 1, 3, ...
 // A softmax thread owns one query row j (TMEM lane 32*(warp%4) + lane).
@@ -44,7 +45,7 @@ struct FwdCfg {
   static constexpr int BM = 128;                   // query rows per tile
   static constexpr int BN = 128;                   // keys per tile
   static constexpr int G = (D == 64) ? 2 : 4;      // rows s per CTA
-  static constexpr int NS = 3;                     // K/V pipeline stages
+  static constexpr int NS = (D == 64) ? 3 : 4;     // K/V pipeline stages
   static constexpr uint32_t ROW = D * 2;           // bytes of one bf16 row
   static constexpr uint32_t ATOM = 8 * ROW;        // swizzle atom (8 rows)
   static constexpr Swizzle SW = D == 16 ? kSw32 : (D == 32 ? kSw64 : kSw128);
@@ -57,7 +58,8 @@ struct FwdCfg {
   static constexpr uint32_t OFF_BIAS = OFF_V + NS * TILE;       // 2 stages, rows = query j
   static constexpr uint32_t OFF_RAW = OFF_BIAS + 2 * BIAS_TILE; // staging of a j-contiguous bias
   static constexpr uint32_t OFF_MADD = OFF_RAW + BIAS_TILE;
-  static constexpr uint32_t SMEM = OFF_MADD + NS * BN * 4;
+  static constexpr uint32_t OFF_FLAG = OFF_MADD + NS * BN * 4;  // per stage: tile has masked keys
+  static constexpr uint32_t SMEM = OFF_FLAG + NS * 16;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
   // tensor memory: S of warpgroup w at 128*w, P of warpgroup w at 256 + 64*w,
   // O of row s at 384 + s*D
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_q, bar_kv_full[C::NS], bar_kv_empty[C::NS], bar_bias_full[2],
-      bar_bias_empty[2], bar_raw, bar_s_full[2], bar_s_free[2], bar_p_ready[2], bar_p_free[2],
+      bar_bias_empty[2], bar_raw, bar_raw_free, bar_s_full[2], bar_s_free[2], bar_p_ready[2], bar_p_free[2],
       bar_o_done[C::G], bar_drain;
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
@@ -119,9 +121,10 @@ __global__ void __launch_bounds__(384, 1)
     abort_flag = 0;
     mbar_init(&bar_q, 1);
     mbar_init(&bar_raw, 1);
+    mbar_init(&bar_raw_free, 2);  // both transposing warps
     for (int i = 0; i < C::NS; ++i) { mbar_init(&bar_kv_full[i], 1); mbar_init(&bar_kv_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_bias_full[i], 1);
+      mbar_init(&bar_bias_full[i], BIAS_K_CONTIG ? 1 : 2);
       mbar_init(&bar_bias_empty[i], 128 * n_wg);
       mbar_init(&bar_s_full[i], 1);
       mbar_init(&bar_s_free[i], 128);
@@ -198,22 +201,11 @@ __global__ void __launch_bounds__(384, 1)
     for (int kt = 0; kt < nkt && ok; ++kt) {
       const int bs = kt & 1;
       uint8_t* stage = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
-      if (kt >= 2) ok = mbar_wait(&bar_bias_empty[bs], ((kt >> 1) - 1) & 1, wctx);
+      if (BIAS_K_CONTIG && kt >= 2) ok = mbar_wait(&bar_bias_empty[bs], ((kt >> 1) - 1) & 1, wctx);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       if (BIAS_K_CONTIG) {
         if (lane == 0) issue_bias(kt, stage, &bar_bias_full[bs]);
-      } else {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw, kt & 1, wctx));
-        if (!ok) break;
-        transpose_tile128_bf16(smem + C::OFF_RAW, stage, lane);
-        fence_proxy_async_smem();  // generic reads of the staging buffer before its next TMA
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bar_bias_full[bs]);
-          if (kt + 1 < nkt) issue_bias(kt + 1, smem + C::OFF_RAW, &bar_raw);
-        }
-        raw_issued = min(kt + 2, nkt);
       }
       bias_issued = kt + 1;
       for (int s = 0; s < g_eff; ++s) {
@@ -222,17 +214,22 @@ __global__ void __launch_bounds__(384, 1)
         if (i >= C::NS) ok = mbar_wait(&bar_kv_empty[st], ((i / C::NS) - 1) & 1, wctx);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        // additive key mask of (s, kt) in log2 units: 0 kept, -1e9*log2(e)
-        // masked, -inf beyond N
+        // additive key mask of (s, kt) in units of the unscaled logit
+        // (S + sqrt(D) bias): 0 kept, -1e9*sqrt(D) masked, -inf beyond N; and a
+        // flag telling the softmax whether the tile has any such key
         float* madd = reinterpret_cast<float*>(smem + C::OFF_MADD + st * C::BN * 4);
+        bool any = false;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int kk = kt * C::BN + e * 32 + lane;
           float a = 0.f;
           if (kk >= p.N) a = -INFINITY;
-          else if (p.mask && !pre_m[e]) a = kMaskBias * kLog2e;
+          else if (p.mask && !pre_m[e]) a = kMaskBias * sqrtf((float)D);
           madd[e * 32 + lane] = a;
+          any |= a != 0.f;
         }
+        any = __any_sync(0xffffffffu, any);
+        if (lane == 0) *reinterpret_cast<int*>(smem + C::OFF_FLAG + st * 16) = any ? 1 : 0;
         prefetch_mask(i + 1);
         __syncwarp();
         if (lane == 0) {
@@ -243,6 +240,14 @@ __global__ void __launch_bounds__(384, 1)
                       s0 + s, b);
         }
         kv_issued = i + 1;
+      }
+      if (!ok) break;
+      if (!BIAS_K_CONTIG && kt + 1 < nkt) {
+        // the staging buffer is free once the transposing warps read tile kt
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw_free, kt & 1, wctx));
+        if (!ok) break;
+        if (lane == 0) issue_bias(kt + 1, smem + C::OFF_RAW, &bar_raw);
+        raw_issued = kt + 2;
       }
     }
     // After a give-up, let every copy already issued land before the CTA may
@@ -269,46 +274,59 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t sq = smem_u32(smem + C::OFF_Q), sk = smem_u32(smem + C::OFF_K),
                      sv = smem_u32(smem + C::OFF_V);
       bool ok = mbar_wait(&bar_q, 0, wctx);
-      // Poll: issue S = QK^T of tile a as soon as its K/V stage is loaded and
-      // its warpgroup has taken its previous S into registers, and O += PV of
-      // tile bq as soon as its P is stored, so neither warpgroup waits for
-      // the other.
-      int a = 0, bq = 0;
-      int n_qk[2] = {0, 0}, n_pv[2] = {0, 0};  // per-warpgroup counts issued
+      // Poll: for each warpgroup independently, issue S = QK^T of its next
+      // tile as soon as that tile's K/V stage is loaded and the warpgroup has
+      // taken its previous S into registers, and O += PV of its oldest tile
+      // as soon as that P is stored; neither warpgroup waits for the other.
+      auto next_same = [&](int i) -> int {  // next iteration of the same warpgroup
+        for (int j = i + 1; j < total; ++j)
+          if (((j % g_eff) & 1) == ((i % g_eff) & 1)) return j;
+        return total;
+      };
+      int qk_next[2] = {0, g_eff >= 2 ? 1 : total};   // next QK tile per warpgroup
+      int pv_next[2] = {0, g_eff >= 2 ? 1 : total};   // next PV tile per warpgroup
+      int n_qk[2] = {0, 0}, n_pv[2] = {0, 0};          // per-warpgroup counts issued
+      int pv_done = 0;
       Watchdog wd;
       wd.reset();
-      while (ok && bq < total) {
+      while (ok && pv_done < total) {
         bool prog = false;
-        if (a < total) {
-          const int s = a % g_eff, st = a % C::NS, w = s & 1;
-          if ((n_qk[w] == 0 || mbar_test(&bar_s_free[w], (n_qk[w] - 1) & 1)) &&
-              mbar_test(&bar_kv_full[st], (a / C::NS) & 1)) {
-            tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              umma_ss(tmem + 128 * w, umma_desc(sq + s * C::TILE + kk * 32, 16, C::ATOM, C::SW),
-                      umma_desc(sk + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_s, kk > 0);
-            umma_commit(&bar_s_full[w]);
-            ++n_qk[w];
-            ++a;
-            prog = true;
+        for (int w = 0; w < 2; ++w) {
+          const int a = qk_next[w];
+          if (a < total) {
+            const int s = a % g_eff, st = a % C::NS;
+            if ((n_qk[w] == 0 || mbar_test(&bar_s_free[w], (n_qk[w] - 1) & 1)) &&
+                mbar_test(&bar_kv_full[st], (a / C::NS) & 1)) {
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                umma_ss(tmem + 128 * w, umma_desc(sq + s * C::TILE + kk * 32, 16, C::ATOM, C::SW),
+                        umma_desc(sk + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_s, kk > 0);
+              umma_commit(&bar_s_full[w]);
+              ++n_qk[w];
+              qk_next[w] = next_same(a);
+              prog = true;
+            }
           }
-        }
-        if (bq < a) {
-          const int kt = bq / g_eff, s = bq % g_eff, st = bq % C::NS, w = s & 1;
-          if (mbar_test(&bar_p_ready[w], n_pv[w] & 1)) {
-            tc_fence_after();
+          const int bq = pv_next[w];
+          if (bq < total && n_pv[w] < n_qk[w]) {
+            const int kt = bq / g_eff, s = bq % g_eff, st = bq % C::NS;
+            if (mbar_test(&bar_p_ready[w], n_pv[w] & 1)) {
+              tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_ts(tmem + C::TMEM_O + s * D, tmem + C::TMEM_P + 64 * w + kk * 8,
-                      umma_desc(sv + st * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_o,
-                      (kt > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&bar_kv_empty[st]);
-            umma_commit(&bar_o_done[s]);
-            umma_commit(&bar_p_free[w]);
-            ++n_pv[w];
-            ++bq;
-            prog = true;
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tmem + C::TMEM_O + s * D, tmem + C::TMEM_P + 64 * w + kk * 8,
+                        umma_desc(sv + st * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_o,
+                        (kt > 0 || kk > 0) ? 1u : 0u);
+              umma_commit(&bar_kv_empty[st]);
+              umma_commit(&bar_o_done[s]);
+              umma_commit(&bar_p_free[w]);
+              ++n_pv[w];
+              ++pv_done;
+              pv_next[w] = next_same(bq);
+              prog = true;
+            }
           }
         }
         if (prog) wd.reset();
@@ -321,7 +339,25 @@ __global__ void __launch_bounds__(384, 1)
     }
     __syncwarp();
   }
-  // warps 2-3 have no role
+  else if (!BIAS_K_CONTIG) {
+    // =================== bias transpose (warps 2-3) =========================
+    const int half = warp - 2;  // each warp moves 128 of the 256 8x8 blocks
+    for (int kt = 0; kt < nkt; ++kt) {
+      const int bs = kt & 1;
+      bool ok = true;
+      if (kt >= 2) ok = mbar_wait(&bar_bias_empty[bs], ((kt >> 1) - 1) & 1, wctx);
+      ok = ok && mbar_wait(&bar_raw, kt & 1, wctx);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      transpose_tile128_bf16(smem + C::OFF_RAW, smem + C::OFF_BIAS + bs * C::BIAS_TILE, lane,
+                             128 * half, 128);
+      fence_proxy_async_smem();  // generic reads of the staging buffer before its next TMA
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar_raw_free);
+        mbar_arrive(&bar_bias_full[bs]);
+      }
+    }
+  }
   teardown();
   } else {
     // =================== softmax warpgroups ================================
@@ -332,8 +368,9 @@ __global__ void __launch_bounds__(384, 1)
     const int j = jt * C::BM + row;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const float c1 = kLog2e * rsqrtf((float)D);      // logit scale in log2 units
-    const float2 c1c1 = make_float2(c1, c1), l2l2 = make_float2(kLog2e, kLog2e);
-    float m_run[C::G / 2], l_run[C::G / 2];
+    const float sqd = sqrtf((float)D);
+    const float2 c1c1 = make_float2(c1, c1), sqd2 = make_float2(sqd, sqd);
+    float m_run[C::G / 2], l_run[C::G / 2];  // running max (t' units) and sum
 #pragma unroll
     for (int u = 0; u < C::G / 2; ++u) { m_run[u] = -INFINITY; l_run[u] = 0.f; }
     bool ok = wg < n_wg;
@@ -362,7 +399,9 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_before();
         mbar_arrive(&bar_s_free[wg]);  // S may now be overwritten by the next QK^T
         const float* madd = reinterpret_cast<const float*>(smem + C::OFF_MADD + st * C::BN * 4);
-        // t = S*c1 + madd + bias*log2(e), in place; 8 independent max chains
+        const bool masked = *reinterpret_cast<const int*>(smem + C::OFF_FLAG + st * 16) != 0;
+        // t' = S + sqrt(D) * bias (+ mask), in place: the logit in log2 units is
+        // c1 * t'.  4 independent max chains.
         float mx[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) mx[e] = -INFINITY;
@@ -370,25 +409,28 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < 16; ++c) {
           const uint4 w4 = *reinterpret_cast<const uint4*>(
               brow + (c >> 3) * (C::BIAS_TILE / 2) + ((((c & 7) ^ (row & 7))) << 4));
-          const float4 ma = *reinterpret_cast<const float4*>(madd + 8 * c);
-          const float4 mb = *reinterpret_cast<const float4*>(madd + 8 * c + 4);
           const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-          const float2 mv[4] = {make_float2(ma.x, ma.y), make_float2(ma.z, ma.w),
-                                make_float2(mb.x, mb.y), make_float2(mb.z, mb.w)};
+          float2 mv[4];
+          if (masked) {  // warp-uniform
+            const float4 ma = *reinterpret_cast<const float4*>(madd + 8 * c);
+            const float4 mb = *reinterpret_cast<const float4*>(madd + 8 * c + 4);
+            mv[0] = make_float2(ma.x, ma.y); mv[1] = make_float2(ma.z, ma.w);
+            mv[2] = make_float2(mb.x, mb.y); mv[3] = make_float2(mb.z, mb.w);
+          }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int k2 = 8 * c + 2 * e;
-            float2 t = fma2(make_float2(__uint_as_float(x[k2]), __uint_as_float(x[k2 + 1])),
-                            c1c1, mv[e]);
-            t = fma2(make_float2(bf16lo(wv[e]), bf16hi(wv[e])), l2l2, t);
+            float2 t = fma2(make_float2(bf16lo(wv[e]), bf16hi(wv[e])), sqd2,
+                            make_float2(__uint_as_float(x[k2]), __uint_as_float(x[k2 + 1])));
+            if (masked) t = add2(t, mv[e]);
             x[k2] = __float_as_uint(t.x);
             x[k2 + 1] = __float_as_uint(t.y);
             mx[e] = fmaxf(mx[e], fmaxf(t.x, t.y));
           }
         }
         const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        const float m_new = fmaxf(m_run[u], rmax);
-        const float alpha = ex2(m_run[u] - m_new);
+        const float m_new = fmaxf(m_run[u], rmax);  // in t' units
+        const float alpha = ex2((m_run[u] - m_new) * c1);
         // rescale O of this row when its running max moved (warp-uniform)
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_o_done[s], (kt - 1) & 1, wctx));
@@ -410,7 +452,7 @@ __global__ void __launch_bounds__(384, 1)
           if (!ok) break;
           tc_fence_after();
         }
-        const float2 negm = make_float2(-m_new, -m_new);
+        const float2 negm = make_float2(-m_new * c1, -m_new * c1);
         float2 sum[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) sum[e] = make_float2(0.f, 0.f);
@@ -420,8 +462,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int k2 = 32 * q4 + 2 * e;
-            const float2 a = add2(make_float2(__uint_as_float(x[k2]), __uint_as_float(x[k2 + 1])),
-                                  negm);
+            const float2 a = fma2(make_float2(__uint_as_float(x[k2]), __uint_as_float(x[k2 + 1])),
+                                  c1c1, negm);
             const float2 pr = make_float2(ex2(a.x), ex2(a.y));
             sum[e & 3] = add2(sum[e & 3], pr);
             pk[e] = pack_bf16(pr.x, pr.y);
@@ -461,7 +503,7 @@ __global__ void __launch_bounds__(384, 1)
           const float inv_l = 1.0f / l_run[u];
           const int ss = s0 + s;
           const int64_t row_id = (((int64_t)b * p.S + ss) * p.H + h) * p.N + j;
-          p.lse[row_id] = (m_run[u] + __log2f(l_run[u])) * kLn2;
+          p.lse[row_id] = (m_run[u] * c1 + __log2f(l_run[u])) * kLn2;
           __nv_bfloat16* dst = p.out + p.o.at(b, ss, h, j, 0);
           const __nv_bfloat16* gsrc = HAS_GATE ? p.gate + p.g.at(b, ss, h, j, 0) : nullptr;
 #pragma unroll
