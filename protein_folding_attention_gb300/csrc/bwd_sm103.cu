@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(384, 1)
 template <int D>
 struct DbiasCfg : Tile<D> {
   using T = Tile<D>;
-  static constexpr int NST = 2;
+  static constexpr int NST = 4;  // (Q, dOa, K, V) stages over s
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_DO = OFF_Q + NST * T::TILE;
   static constexpr uint32_t OFF_K = OFF_DO + NST * T::TILE;
@@ -675,6 +675,7 @@ struct DbiasCfg : Tile<D> {
   static constexpr uint32_t OFF_MADD = OFF_RAW + T::BIAS_TILE;
   static constexpr uint32_t SMEM = OFF_MADD + NST * 128 * 4;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory overflow");
   static constexpr uint32_t T_S = 0, T_DP = 128;
   static constexpr int THREADS = 384;
   static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 224;
