@@ -104,6 +104,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(seconds: float, dist=None, device=None) -> float:
+    """Slowest rank's time (the job's time); identity without a process group."""
+    if dist is None:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world_size: int, seconds_per_step: float) -> float:
+    """Whole-job throughput: every rank's FLOP over the slowest rank's step time."""
+    return flops_per_rank * world_size / seconds_per_step / 1e12
+
+
 def config_block(w):
     return {"workload": w.name, "B": w.B, "S": w.S, "N": w.N, "H": w.H, "D": w.D,
             "node": w.node, "mask": f"{w.mask_tail} trailing keys masked" if w.mask == "tail"
@@ -210,7 +225,13 @@ def run_ours(args, w):
     status = evoattn.device_status()
     if status != evoattn.OK:
         raise RuntimeError(f"device status {status} after warm-up")
-    peak_extra = torch.cuda.max_memory_allocated(dev) - mem0
+    # The library allocates nothing: everything on the device is the caller's
+    # inputs, outputs and the backward workspace (linear in B*S*H*N*D plus
+    # O(B*H*N^2)); the logits are never stored.
+    memory = {"device_bytes_in_use": int(torch.cuda.max_memory_allocated(dev)),
+              "growth_during_steps_bytes": int(torch.cuda.max_memory_allocated(dev) - mem0),
+              "bwd_workspace_bytes": int(wsp.numel()),
+              "logits_bytes_if_materialized_bf16": int(w.logits * 2)}
 
     # ---- timed region: K steps, per-kernel events on the launching stream ----
     n_ev = 5
@@ -229,11 +250,7 @@ def run_ours(args, w):
             bwd(ev_b[i])
         t1.record(stream)
         barrier()
-    elapsed = t0.elapsed_time(t1) * 1e-3
-    if pg is not None:
-        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(t0.elapsed_time(t1) * 1e-3, pg, dev)
     status = evoattn.device_status()
     if status != evoattn.OK:
         raise RuntimeError(f"device status {status} in timed region")
@@ -244,7 +261,7 @@ def run_ours(args, w):
     t_bwd = sum(stage)
     step = elapsed / args.steps
     total_flops = (w.fwd_flops + w.bwd_flops) * ws
-    value = total_flops / step / 1e12
+    value = job_tflops(w.fwd_flops + w.bwd_flops, ws, step)
     peak = peaks["bf16_tflops"]
 
     # ---- end to end: pinned host inputs -> device, fwd+bwd, results -> host
@@ -278,11 +295,7 @@ def run_ours(args, w):
             e2e_step()
         e1.record(stream)
         barrier()
-        te = e0.elapsed_time(e1) * 1e-3 / ksteps
-        if pg is not None:
-            t = torch.tensor([te], device=dev, dtype=torch.float64)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            te = float(t.item())
+        te = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / ksteps, pg, dev)
         e2e = {"value": total_flops / te / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3}
 
@@ -327,7 +340,7 @@ def run_ours(args, w):
                                           [s * 1e3 for s in stage]))},
             "peak_tflops": peak, "peak_source": peak_src,
             "frac_of_peak": value / ws / peak,
-            "peak_mem_extra_bytes": int(peak_extra),
+            "memory": memory,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks.summary(),
             "gpu_launches": args.steps * 6,
@@ -362,7 +375,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--ref-rows", type=int, default=16,
                     help="s rows per step of the --impl reference arm")
-    ap.add_argument("--cpu-rows", type=int, default=48,
+    ap.add_argument("--cpu-rows", type=int, default=192,
                     help="s rows of the cpu_baseline sample")
     ap.add_argument("--s-rows", type=int, default=0,
                     help="profiling only: truncate the workload to this many s rows")

@@ -1,0 +1,66 @@
+"""Host-side logic of bench.py without a GPU: clock-sample parsing, the
+committed traffic table, the whole-job aggregation over ranks (world size 2
+on gloo), and the JSON line of the --impl reference arm on the tiny workload."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_clock_summary_parses_nvidia_smi_lines():
+    c = bench.ClockSampler(0)
+    c.lines = ["0, 1950, 2070, 1200.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+               "0, 2070, 2070, 1300.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+               "0, 345, 2070, 300.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active"]
+    s = c.summary()
+    assert s["sm_max_mhz"] == 2070.0
+    assert s["sm_mhz"] == pytest.approx(2010.0)   # median of the loaded samples
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_traffic_table_lookup():
+    assert bench.profiled_traffic("k_dkdv", "pairformer_end_n768") > 1e8
+    assert bench.profiled_traffic("k_dkdv", "no_such_workload") is None
+
+
+def _ranks(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t = bench.max_over_ranks(1.0 + rank, dist)        # rank 1 is the slowest
+    q.put((rank, t, bench.job_tflops(2e12, world, t)))
+    dist.destroy_process_group()
+
+
+def test_job_time_is_max_over_ranks_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_ranks, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    out = sorted(q.get() for _ in range(2))
+    assert [t for _, t, _ in out] == [2.0, 2.0]
+    assert out[0][2] == pytest.approx(2e12 * 2 / 2.0 / 1e12)
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_start_n32_fp32", "--steps", "1", "--warmup", "0",
+                        "--ref-rows", "4"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
