@@ -311,23 +311,30 @@ __global__ void __launch_bounds__(384, 1)
     // The compute threads read the bias tile by key rows.  A key-row-major
     // tile (queries contiguous: the ending-node view) is fetched straight
     // into its stage; a query-row-major one is staged and transposed.
+    // Copies issued by one thread are served in order, those of different
+    // threads concurrently: each box is issued by the next lane in turn (the
+    // whole warp calls issue_bias; lane 0 arms the barrier first).
+    int rr = 0;
     auto issue_bias = [&](int g, uint8_t* dst, uint64_t* bar) {
       const DkdvItem it = item(g / njt);
       const int jt = g % njt;
-      mbar_arrive_expect_tx(bar, C::BIAS_TILE);
+      if (lane == 0) mbar_arrive_expect_tx(bar, C::BIAS_TILE);
+      __syncwarp();
+      const int l0 = rr & 31, l1 = (rr + 1) & 31;
+      rr += 2;
       if (BIAS_K_CONTIG) {
-        tma_load_4d(dst, &tm_bias, bar, it.kt * 128, jt * 128, it.h, it.b);
-        tma_load_4d(dst + 16384, &tm_bias, bar, it.kt * 128 + 64, jt * 128, it.h, it.b);
+        if (lane == l0) tma_load_4d(dst, &tm_bias, bar, it.kt * 128, jt * 128, it.h, it.b);
+        if (lane == l1) tma_load_4d(dst + 16384, &tm_bias, bar, it.kt * 128 + 64, jt * 128, it.h, it.b);
       } else {
-        tma_load_4d(dst, &tm_bias, bar, jt * 128, it.kt * 128, it.h, it.b);
-        tma_load_4d(dst + 16384, &tm_bias, bar, jt * 128 + 64, it.kt * 128, it.h, it.b);
+        if (lane == l0) tma_load_4d(dst, &tm_bias, bar, jt * 128, it.kt * 128, it.h, it.b);
+        if (lane == l1) tma_load_4d(dst + 16384, &tm_bias, bar, jt * 128 + 64, it.kt * 128, it.h, it.b);
       }
     };
     const float inv_sqrt_d = rsqrtf((float)D);
     bool ok = true;
     int kv_issued = 0, qd_issued = 0, b_issued = 0, raw_issued = 0;
     if (BIAS_K_CONTIG && total > 0) {
-      if (lane == 0) issue_bias(0, smem + C::OFF_RAW, &bar_raw);
+      issue_bias(0, smem + C::OFF_RAW, &bar_raw);
       raw_issued = 1;
     }
     // The per-query constants of tile g+1 are loaded into registers while
@@ -352,13 +359,15 @@ __global__ void __launch_bounds__(384, 1)
       if (n >= 2) ok = mbar_wait(&bar_kv_empty[kvs], ((n >> 1) - 1) & 1, wctx);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bar_kv_full[kvs], 2 * C::TILE);
+      if (lane == 0) mbar_arrive_expect_tx(&bar_kv_full[kvs], 2 * C::TILE);
+      __syncwarp();
+      if (lane == (rr & 31))
         tma_load_5d(smem + C::OFF_K + kvs * C::TILE, &tm_k, &bar_kv_full[kvs], 0, it.kt * 128,
                     it.h, it.s, it.b);
+      if (lane == ((rr + 1) & 31))
         tma_load_5d(smem + C::OFF_V + kvs * C::TILE, &tm_v, &bar_kv_full[kvs], 0, it.kt * 128,
                     it.h, it.s, it.b);
-      }
+      rr += 2;
       kv_issued = n + 1;
       for (int jt = 0; jt < njt; ++jt, ++g) {
         const int qs = g % C::NQ, bs = g % C::NB;
@@ -367,13 +376,15 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         // Q and dOa tiles first; the phase completes only with the arrival
         // after the per-query constants below
-        if (lane == 0) {
-          mbar_expect_tx(&bar_qd_full[qs], 2 * C::TILE);
+        if (lane == 0) mbar_expect_tx(&bar_qd_full[qs], 2 * C::TILE);
+        __syncwarp();
+        if (lane == (rr & 31))
           tma_load_5d(smem + C::OFF_Q + qs * C::TILE, &tm_q, &bar_qd_full[qs], 0, jt * 128, it.h,
                       it.s, it.b);
+        if (lane == ((rr + 1) & 31))
           tma_load_5d(smem + C::OFF_DO + qs * C::TILE, &tm_do, &bar_qd_full[qs], 0, jt * 128,
                       it.h, it.s, it.b);
-        }
+        rr += 2;
         // per-query constants of this tile, negated: -lse in log2 units
         // (-inf beyond N so that P = 0 there) and -delta / sqrt(D)
         float* ld = reinterpret_cast<float*>(smem + C::OFF_LD + qs * 1024);
@@ -392,7 +403,7 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         uint8_t* stage = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
         if (!BIAS_K_CONTIG) {
-          if (lane == 0) issue_bias(g, stage, &bar_b_full[bs]);
+          issue_bias(g, stage, &bar_b_full[bs]);
           b_issued = g + 1;
         } else {
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw, g & 1, wctx));
@@ -400,10 +411,8 @@ __global__ void __launch_bounds__(384, 1)
           transpose_tile128_bf16(smem + C::OFF_RAW, stage, lane);
           fence_proxy_async_smem();  // generic reads of the staging buffer before its next TMA
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&bar_b_full[bs]);
-            if (g + 1 < total) issue_bias(g + 1, smem + C::OFF_RAW, &bar_raw);
-          }
+          if (lane == 0) mbar_arrive(&bar_b_full[bs]);
+          if (g + 1 < total) issue_bias(g + 1, smem + C::OFF_RAW, &bar_raw);
           if (g + 1 < total) raw_issued = g + 2;
         }
       }
@@ -428,61 +437,69 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t id_sdp = idesc_bf16(128, 128, 0, 0);  // A=K/V, B=Q/dOa, K-major
       constexpr uint32_t id_kv = idesc_bf16(128, D, 0, 1);     // A=P^T/dS^T (TMEM), B MN-major
       constexpr uint32_t id_q = idesc_bf16(128, D, 1, 1);      // A=dS (smem, MN-major)
-      const uint32_t sk = smem_u32(smem + C::OFF_K), sv = smem_u32(smem + C::OFF_V),
-                     sq = smem_u32(smem + C::OFF_Q), sdo = smem_u32(smem + C::OFF_DO),
-                     sds = smem_u32(smem + C::OFF_DS);
-      int a = 0, bq = 0;  // next S/dP tile, next dV/dK/dQ tile
+      // A single thread issues every MMA, so its own instruction latency
+      // paces the tensor core: descriptors are built once and offset by
+      // constants, and tile bookkeeping uses additions only.
+      const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
+      const uint64_t dv0 = umma_desc(smem_u32(smem + C::OFF_V), 16, C::ATOM, C::SW);
+      const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
+      const uint64_t ddo0 = umma_desc(smem_u32(smem + C::OFF_DO), 16, C::ATOM, C::SW);
+      const uint64_t dds0 = umma_desc(smem_u32(smem + C::OFF_DS), 16384, 1024, kSw128);
+      constexpr uint32_t TILE16 = C::TILE >> 4, KSTEP16 = (16 * C::ROW) >> 4;
+      // cursors: tile index, its query tile jt, its item n, Q/dO stage, phase
+      struct Cur { int t, jt, n, qs, qph; };
+      auto advance = [&](Cur& c) {
+        ++c.t;
+        if (++c.jt == njt) { c.jt = 0; ++c.n; }
+        if (++c.qs == C::NQ) { c.qs = 0; c.qph ^= 1; }
+      };
+      Cur ca{0, 0, 0, 0, 0}, cb{0, 0, 0, 0, 0};  // next S/dP tile, next dV/dK/dQ tile
       Watchdog wd;
       wd.reset();
       bool ok = true;
-      while (bq < total) {
+      while (cb.t < total) {
         bool prog = false;
-        if (a < total && a <= bq + 1) {
-          const int n = a / njt, jt = a % njt, qs = a % C::NQ, kvs = n & 1;
-          if ((a == 0 || mbar_test(&bar_sdp_free, (a - 1) & 1)) &&
-              mbar_test(&bar_qd_full[qs], (a / C::NQ) & 1) &&
-              (jt != 0 || mbar_test(&bar_kv_full[kvs], (n >> 1) & 1))) {
+        if (ca.t < total && ca.t <= cb.t + 1) {
+          const int kvs = ca.n & 1;
+          if ((ca.t == 0 || mbar_test(&bar_sdp_free, (ca.t - 1) & 1)) &&
+              mbar_test(&bar_qd_full[ca.qs], ca.qph) &&
+              (ca.jt != 0 || mbar_test(&bar_kv_full[kvs], (ca.n >> 1) & 1))) {
             tc_fence_after();
+            const uint64_t dk = dk0 + kvs * TILE16, dv = dv0 + kvs * TILE16;
+            const uint64_t dq = dq0 + ca.qs * TILE16, ddo = ddo0 + ca.qs * TILE16;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              umma_ss(tmem + C::T_S, umma_desc(sk + kvs * C::TILE + kk * 32, 16, C::ATOM, C::SW),
-                      umma_desc(sq + qs * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_sdp, kk > 0);
-              umma_ss(tmem + C::T_DP, umma_desc(sv + kvs * C::TILE + kk * 32, 16, C::ATOM, C::SW),
-                      umma_desc(sdo + qs * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_sdp,
-                      kk > 0);
+              umma_ss(tmem + C::T_S, dk + 2 * kk, dq + 2 * kk, id_sdp, kk > 0);
+              umma_ss(tmem + C::T_DP, dv + 2 * kk, ddo + 2 * kk, id_sdp, kk > 0);
             }
             umma_commit(&bar_s_full);
-            ++a;
+            advance(ca);
             prog = true;
           }
         }
-        if (bq < a) {
-          const int n = bq / njt, jt = bq % njt, qs = bq % C::NQ, kvs = n & 1;
+        if (cb.t < ca.t) {
+          const int kvs = cb.n & 1, bq = cb.t;
           if (mbar_test(&bar_p_ready, bq & 1) &&
               (bq < 2 || mbar_test(&bar_dq_free[bq & 1], ((bq >> 1) - 1) & 1)) &&
-              (jt != 0 || n == 0 || mbar_test(&bar_dkdv_free, (n - 1) & 1))) {
+              (cb.jt != 0 || cb.n == 0 || mbar_test(&bar_dkdv_free, (cb.n - 1) & 1))) {
             tc_fence_after();
+            const uint64_t dq = dq0 + cb.qs * TILE16, ddo = ddo0 + cb.qs * TILE16;
+            const uint64_t dk = dk0 + kvs * TILE16;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t acc = (jt > 0 || kk > 0) ? 1u : 0u;
+              const uint32_t acc = (cb.jt > 0 || kk > 0) ? 1u : 0u;
               // dV += P^T dOa ; dK += dS^T Q  (K dimension = queries, 16 per step)
-              umma_ts(tmem + C::T_DV, tmem + C::T_P + kk * 8,
-                      umma_desc(sdo + qs * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_kv,
-                      acc);
-              umma_ts(tmem + C::T_DK, tmem + C::T_DS + kk * 8,
-                      umma_desc(sq + qs * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_kv,
-                      acc);
+              umma_ts(tmem + C::T_DV, tmem + C::T_P + kk * 8, ddo + kk * KSTEP16, id_kv, acc);
+              umma_ts(tmem + C::T_DK, tmem + C::T_DS + kk * 8, dq + kk * KSTEP16, id_kv, acc);
             }
+            const uint32_t dqt = tmem + C::T_DQ + (bq & 1) * D;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K dimension = keys)
-              umma_ss(tmem + C::T_DQ + (bq & 1) * D,
-                      umma_desc(sds + kk * 2048, 16384, 1024, kSw128),
-                      umma_desc(sk + kvs * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_q,
-                      kk > 0);
-            umma_commit(&bar_qd_empty[qs]);
-            if (jt == njt - 1) umma_commit(&bar_kv_empty[kvs]);
+              umma_ss(dqt, dds0 + kk * (2048 >> 4), dk + kk * KSTEP16, id_q, kk > 0);
+            umma_commit(&bar_qd_empty[cb.qs]);
+            if (cb.jt == njt - 1) umma_commit(&bar_kv_empty[kvs]);
             umma_commit(&bar_mma_done);
-            ++bq;
+            advance(cb);
             prog = true;
           }
         }
@@ -756,16 +773,19 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {
     // ============================ producer =================================
     bool ok = true;
-    if (lane == 0) {
+    {
+      // copies issued by one thread are served in order, those of different
+      // threads concurrently: each box goes out from its own lane
       uint8_t* dst = smem + (BIAS_K_CONTIG ? C::OFF_BIAS : C::OFF_RAW);
       uint64_t* bar = BIAS_K_CONTIG ? &bar_bias : &bar_raw;
-      mbar_arrive_expect_tx(bar, C::BIAS_TILE);
+      if (lane == 0) mbar_arrive_expect_tx(bar, C::BIAS_TILE);
+      __syncwarp();
       if (BIAS_K_CONTIG) {
-        tma_load_4d(dst, &tm_bias, bar, kt * 128, jt * 128, h, b);
-        tma_load_4d(dst + 16384, &tm_bias, bar, kt * 128 + 64, jt * 128, h, b);
+        if (lane == 0) tma_load_4d(dst, &tm_bias, bar, kt * 128, jt * 128, h, b);
+        if (lane == 1) tma_load_4d(dst + 16384, &tm_bias, bar, kt * 128 + 64, jt * 128, h, b);
       } else {
-        tma_load_4d(dst, &tm_bias, bar, jt * 128, kt * 128, h, b);
-        tma_load_4d(dst + 16384, &tm_bias, bar, jt * 128 + 64, kt * 128, h, b);
+        if (lane == 0) tma_load_4d(dst, &tm_bias, bar, jt * 128, kt * 128, h, b);
+        if (lane == 1) tma_load_4d(dst + 16384, &tm_bias, bar, jt * 128 + 64, kt * 128, h, b);
       }
     }
     int issued = 0;
@@ -797,12 +817,18 @@ __global__ void __launch_bounds__(384, 1)
       }
       prefetch_mask(i + 1);
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bar_full[st], 4 * C::TILE);
-        tma_load_5d(smem + C::OFF_Q + st * C::TILE, &tm_q, &bar_full[st], 0, jt * 128, h, s, b);
-        tma_load_5d(smem + C::OFF_DO + st * C::TILE, &tm_do, &bar_full[st], 0, jt * 128, h, s, b);
-        tma_load_5d(smem + C::OFF_K + st * C::TILE, &tm_k, &bar_full[st], 0, kt * 128, h, s, b);
-        tma_load_5d(smem + C::OFF_V + st * C::TILE, &tm_v, &bar_full[st], 0, kt * 128, h, s, b);
+      if (lane == 0) mbar_arrive_expect_tx(&bar_full[st], 4 * C::TILE);
+      __syncwarp();
+      {
+        const int l0 = (2 + 4 * i) & 31;  // lanes 0-1 issued the bias
+        if (lane == l0)
+          tma_load_5d(smem + C::OFF_Q + st * C::TILE, &tm_q, &bar_full[st], 0, jt * 128, h, s, b);
+        if (lane == ((l0 + 1) & 31))
+          tma_load_5d(smem + C::OFF_DO + st * C::TILE, &tm_do, &bar_full[st], 0, jt * 128, h, s, b);
+        if (lane == ((l0 + 2) & 31))
+          tma_load_5d(smem + C::OFF_K + st * C::TILE, &tm_k, &bar_full[st], 0, kt * 128, h, s, b);
+        if (lane == ((l0 + 3) & 31))
+          tma_load_5d(smem + C::OFF_V + st * C::TILE, &tm_v, &bar_full[st], 0, kt * 128, h, s, b);
       }
       issued = i + 1;
       if (!BIAS_K_CONTIG && i == 0) {
@@ -825,8 +851,10 @@ __global__ void __launch_bounds__(384, 1)
     // ============================ MMA issuer ===============================
     if (lane == 0) {
       constexpr uint32_t id = idesc_bf16(128, 128, 0, 0);
-      const uint32_t sq = smem_u32(smem + C::OFF_Q), sdo = smem_u32(smem + C::OFF_DO),
-                     sk = smem_u32(smem + C::OFF_K), sv = smem_u32(smem + C::OFF_V);
+      const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
+      const uint64_t ddo0 = umma_desc(smem_u32(smem + C::OFF_DO), 16, C::ATOM, C::SW);
+      const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
+      const uint64_t dv0 = umma_desc(smem_u32(smem + C::OFF_V), 16, C::ATOM, C::SW);
       bool ok = true;
       for (int i = 0; i < ns && ok; ++i) {
         const int st = i % C::NST;
@@ -834,12 +862,11 @@ __global__ void __launch_bounds__(384, 1)
         if (ok && i > 0) ok = mbar_wait(&bar_sdp_free, (i - 1) & 1, wctx);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t off = (uint32_t)(st * C::TILE) >> 4;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          umma_ss(tmem + C::T_S, umma_desc(sq + st * C::TILE + kk * 32, 16, C::ATOM, C::SW),
-                  umma_desc(sk + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id, kk > 0);
-          umma_ss(tmem + C::T_DP, umma_desc(sdo + st * C::TILE + kk * 32, 16, C::ATOM, C::SW),
-                  umma_desc(sv + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id, kk > 0);
+          umma_ss(tmem + C::T_S, dq0 + off + 2 * kk, dk0 + off + 2 * kk, id, kk > 0);
+          umma_ss(tmem + C::T_DP, ddo0 + off + 2 * kk, dv0 + off + 2 * kk, id, kk > 0);
         }
         umma_commit(&bar_empty[st]);
         umma_commit(&bar_s_full);

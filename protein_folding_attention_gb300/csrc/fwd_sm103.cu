@@ -167,22 +167,33 @@ __global__ void __launch_bounds__(384, 1)
     // A query-row-major bias tile ([j][k], keys contiguous) goes straight to
     // its stage; a key-row-major one (the ending-node view) lands in a
     // staging buffer and the warp transposes it into the stage.
+    // The copy engine serves the copies one thread issues in order, but
+    // those of different threads concurrently; with 64-byte rows a single
+    // issuing thread would cap the loads at ~10 bytes/clock.  Each box is
+    // therefore issued by the next lane of the warp in turn (the whole warp
+    // calls these helpers; lane 0 arms the barrier first).
+    int rr = 0;
     auto issue_bias = [&](int kt, uint8_t* dst, uint64_t* bar) {
-      mbar_arrive_expect_tx(bar, C::BIAS_TILE);
+      if (lane == 0) mbar_arrive_expect_tx(bar, C::BIAS_TILE);
+      __syncwarp();
+      const int l0 = rr & 31, l1 = (rr + 1) & 31;
+      rr += 2;
       if (BIAS_K_CONTIG) {
-        tma_load_4d(dst, &tm_bias, bar, kt * C::BN, jt * C::BM, h, b);
-        tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, bar, kt * C::BN + 64, jt * C::BM, h, b);
+        if (lane == l0) tma_load_4d(dst, &tm_bias, bar, kt * C::BN, jt * C::BM, h, b);
+        if (lane == l1)
+          tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, bar, kt * C::BN + 64, jt * C::BM, h, b);
       } else {
-        tma_load_4d(dst, &tm_bias, bar, jt * C::BM, kt * C::BN, h, b);
-        tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, bar, jt * C::BM + 64, kt * C::BN, h, b);
+        if (lane == l0) tma_load_4d(dst, &tm_bias, bar, jt * C::BM, kt * C::BN, h, b);
+        if (lane == l1)
+          tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, bar, jt * C::BM + 64, kt * C::BN, h, b);
       }
     };
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bar_q, g_eff * C::TILE);
-      for (int s = 0; s < g_eff; ++s)
-        tma_load_5d(smem + C::OFF_Q + s * C::TILE, &tm_q, &bar_q, 0, jt * C::BM, h, s0 + s, b);
-      if (!BIAS_K_CONTIG) issue_bias(0, smem + C::OFF_RAW, &bar_raw);
-    }
+    if (lane == 0) mbar_arrive_expect_tx(&bar_q, g_eff * C::TILE);
+    __syncwarp();
+    if (lane < g_eff)
+      tma_load_5d(smem + C::OFF_Q + lane * C::TILE, &tm_q, &bar_q, 0, jt * C::BM, h, s0 + lane, b);
+    rr = g_eff;
+    if (!BIAS_K_CONTIG) issue_bias(0, smem + C::OFF_RAW, &bar_raw);
     bool ok = true;
     int kv_issued = 0, bias_issued = 0, raw_issued = BIAS_K_CONTIG ? 0 : 1;
     // mask bytes of the next (kt, s) are loaded while the current is armed
@@ -205,7 +216,7 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       if (BIAS_K_CONTIG) {
-        if (lane == 0) issue_bias(kt, stage, &bar_bias_full[bs]);
+        issue_bias(kt, stage, &bar_bias_full[bs]);
       }
       bias_issued = kt + 1;
       for (int s = 0; s < g_eff; ++s) {
@@ -232,13 +243,15 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) *reinterpret_cast<int*>(smem + C::OFF_FLAG + st * 16) = any ? 1 : 0;
         prefetch_mask(i + 1);
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_kv_full[st], 2 * C::TILE);
+        if (lane == 0) mbar_arrive_expect_tx(&bar_kv_full[st], 2 * C::TILE);
+        __syncwarp();
+        if (lane == (rr & 31))
           tma_load_5d(smem + C::OFF_K + st * C::TILE, &tm_k, &bar_kv_full[st], 0, kt * C::BN, h,
                       s0 + s, b);
+        if (lane == ((rr + 1) & 31))
           tma_load_5d(smem + C::OFF_V + st * C::TILE, &tm_v, &bar_kv_full[st], 0, kt * C::BN, h,
                       s0 + s, b);
-        }
+        rr += 2;
         kv_issued = i + 1;
       }
       if (!ok) break;
@@ -246,7 +259,7 @@ __global__ void __launch_bounds__(384, 1)
         // the staging buffer is free once the transposing warps read tile kt
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw_free, kt & 1, wctx));
         if (!ok) break;
-        if (lane == 0) issue_bias(kt + 1, smem + C::OFF_RAW, &bar_raw);
+        issue_bias(kt + 1, smem + C::OFF_RAW, &bar_raw);
         raw_issued = kt + 2;
       }
     }
@@ -271,21 +284,31 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q, K both K-major
       constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);    // P from TMEM, V MN-major
-      const uint32_t sq = smem_u32(smem + C::OFF_Q), sk = smem_u32(smem + C::OFF_K),
-                     sv = smem_u32(smem + C::OFF_V);
+      // A single thread issues every MMA, so its own instruction latency
+      // paces the tensor core: descriptors are built once and offset by
+      // constants, and tile bookkeeping uses additions only.
+      const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
+      const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
+      const uint64_t dv0 = umma_desc(smem_u32(smem + C::OFF_V), 16, C::ATOM, C::SW);
       bool ok = mbar_wait(&bar_q, 0, wctx);
       // Poll: for each warpgroup independently, issue S = QK^T of its next
       // tile as soon as that tile's K/V stage is loaded and the warpgroup has
       // taken its previous S into registers, and O += PV of its oldest tile
       // as soon as that P is stored; neither warpgroup waits for the other.
-      auto next_same = [&](int i) -> int {  // next iteration of the same warpgroup
-        for (int j = i + 1; j < total; ++j)
-          if (((j % g_eff) & 1) == ((i % g_eff) & 1)) return j;
-        return total;
+      // A cursor walks the tiles (kt, s) of one warpgroup: s = w, w+2, ...
+      struct Cur { int a, kt, s; };
+      auto advance = [&](Cur& c, int w) {
+        c.s += 2;
+        if (c.s >= g_eff) { c.s = w; ++c.kt; }
+        c.a = c.kt * g_eff + c.s;
       };
-      int qk_next[2] = {0, g_eff >= 2 ? 1 : total};   // next QK tile per warpgroup
-      int pv_next[2] = {0, g_eff >= 2 ? 1 : total};   // next PV tile per warpgroup
-      int n_qk[2] = {0, 0}, n_pv[2] = {0, 0};          // per-warpgroup counts issued
+      Cur qc[2], pc[2];
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        qc[w] = Cur{w, w < g_eff ? 0 : nkt, w};
+        pc[w] = qc[w];
+      }
+      int n_qk[2] = {0, 0}, n_pv[2] = {0, 0};  // per-warpgroup counts issued
       int pv_done = 0;
       Watchdog wd;
       wd.reset();
@@ -293,40 +316,39 @@ __global__ void __launch_bounds__(384, 1)
         bool prog = false;
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
-          const int a = qk_next[w];
-          if (a < total) {
-            const int s = a % g_eff, st = a % C::NS;
+          Cur& c = qc[w];
+          if (c.kt < nkt) {
+            const int st = c.a % C::NS;
             if ((n_qk[w] == 0 || mbar_test(&bar_s_free[w], (n_qk[w] - 1) & 1)) &&
-                mbar_test(&bar_kv_full[st], (a / C::NS) & 1)) {
+                mbar_test(&bar_kv_full[st], (c.a / C::NS) & 1)) {
               tc_fence_after();
+              const uint64_t dq = dq0 + ((uint32_t)(c.s * C::TILE) >> 4);
+              const uint64_t dk = dk0 + ((uint32_t)(st * C::TILE) >> 4);
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk)
-                umma_ss(tmem + 128 * w, umma_desc(sq + s * C::TILE + kk * 32, 16, C::ATOM, C::SW),
-                        umma_desc(sk + st * C::TILE + kk * 32, 16, C::ATOM, C::SW), id_s, kk > 0);
+                umma_ss(tmem + 128 * w, dq + 2 * kk, dk + 2 * kk, id_s, kk > 0);
               umma_commit(&bar_s_full[w]);
               ++n_qk[w];
-              qk_next[w] = next_same(a);
+              advance(c, w);
               prog = true;
             }
           }
-          const int bq = pv_next[w];
-          if (bq < total && n_pv[w] < n_qk[w]) {
-            const int kt = bq / g_eff, s = bq % g_eff, st = bq % C::NS;
-            if (mbar_test(&bar_p_ready[w], n_pv[w] & 1)) {
-              tc_fence_after();
+          Cur& e = pc[w];
+          if (e.kt < nkt && n_pv[w] < n_qk[w] && mbar_test(&bar_p_ready[w], n_pv[w] & 1)) {
+            const int st = e.a % C::NS;
+            tc_fence_after();
+            const uint64_t dv = dv0 + ((uint32_t)(st * C::TILE) >> 4);
+            const uint32_t o = tmem + C::TMEM_O + e.s * D, pa = tmem + C::TMEM_P + 64 * w;
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                umma_ts(tmem + C::TMEM_O + s * D, tmem + C::TMEM_P + 64 * w + kk * 8,
-                        umma_desc(sv + st * C::TILE + kk * 16 * C::ROW, 16, C::ATOM, C::SW), id_o,
-                        (kt > 0 || kk > 0) ? 1u : 0u);
-              umma_commit(&bar_kv_empty[st]);
-              umma_commit(&bar_o_done[s]);
-              umma_commit(&bar_p_free[w]);
-              ++n_pv[w];
-              ++pv_done;
-              pv_next[w] = next_same(bq);
-              prog = true;
-            }
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ts(o, pa + kk * 8, dv + kk * (16 * C::ROW >> 4), id_o, (e.kt > 0 || kk > 0) ? 1u : 0u);
+            umma_commit(&bar_kv_empty[st]);
+            umma_commit(&bar_o_done[e.s]);
+            umma_commit(&bar_p_free[w]);
+            ++n_pv[w];
+            ++pv_done;
+            advance(e, w);
+            prog = true;
           }
         }
         if (prog) wd.reset();
@@ -370,6 +392,7 @@ __global__ void __launch_bounds__(384, 1)
     const float c1 = kLog2e * rsqrtf((float)D);      // logit scale in log2 units
     const float sqd = sqrtf((float)D);
     const float2 c1c1 = make_float2(c1, c1), sqd2 = make_float2(sqd, sqd);
+    const float lazy_thr = 8.0f / c1;                // 8 in log2 units, in t' units
     float m_run[C::G / 2], l_run[C::G / 2];  // running max (t' units) and sum
 #pragma unroll
     for (int u = 0; u < C::G / 2; ++u) { m_run[u] = -INFINITY; l_run[u] = 0.f; }
@@ -425,11 +448,15 @@ __global__ void __launch_bounds__(384, 1)
             if (masked) t = add2(t, mv[e]);
             x[k2] = __float_as_uint(t.x);
             x[k2 + 1] = __float_as_uint(t.y);
-            mx[e] = fmaxf(mx[e], fmaxf(t.x, t.y));
+            mx[e] = fmax3(mx[e], t.x, t.y);
           }
         }
         const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        const float m_new = fmaxf(m_run[u], rmax);  // in t' units
+        // The reference max m moves only when the tile's max exceeds it by
+        // more than 2^8 in probability (8 in log2 units): P then stays <= 256,
+        // exact in fp32 and at full relative precision in bf16, and most
+        // tiles skip the O rescale.  Any m gives the same softmax.
+        const float m_new = rmax > m_run[u] + lazy_thr ? rmax : m_run[u];  // t' units
         const float alpha = ex2((m_run[u] - m_new) * c1);
         // rescale O of this row when its running max moved (warp-uniform)
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
