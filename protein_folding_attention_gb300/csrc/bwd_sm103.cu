@@ -459,7 +459,10 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       while (cb.t < total) {
         bool prog = false;
-        if (ca.t < total && ca.t <= cb.t + 1) {
+        // S/dP of tile t+1 go out as soon as the compute threads hold S/dP of
+        // tile t, ahead of dV/dK/dQ of tile t: the tensor core then computes
+        // them while tile t's softmax runs (Q/dO stages: t, t+1 and t+2 live)
+        if (ca.t < total && ca.t <= cb.t + 2) {
           const int kvs = ca.n & 1;
           if ((ca.t == 0 || mbar_test(&bar_sdp_free, (ca.t - 1) & 1)) &&
               mbar_test(&bar_qd_full[ca.qs], ca.qph) &&

@@ -14,17 +14,20 @@
 // Warp roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: Q tiles, the bias tile of each kt, K/V tiles of
 //               each (kt, s) and the additive key mask of that (s, kt)
-//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM, O += P V with
-//               P read from TMEM
-//   warps 2-3   transpose a key-row-major (query-contiguous) bias tile into
+//   warps 1-2   MMA issuers, one thread each, warp 1 for softmax warpgroup 0
+//               and warp 2 for warpgroup 1: S = Q K^T into TMEM, O += P V
+//               with P read from TMEM.  An issuing thread spends ~50 cycles
+//               per tcgen05.mma, longer than an N = 32 MMA runs on the tensor
+//               core, so two issuers keep it fed
+//   warp 3      transposes a key-row-major (query-contiguous) bias tile into
 //               query rows; idle otherwise
 //   warps 4-7   softmax warpgroup 0: rows s = 0, 2, ... of the group
 //   warps 8-11  softmax warpgroup 1: rows s = 1, 3, ...
 // A softmax thread owns one query row j (TMEM lane 32*(warp%4) + lane).
 //
 // Tensor memory (512 columns): S buffer of warpgroup w at columns 128*w (fp32
-// 128x128; the bf16 P overwrites its first 64 columns), O of row s at
-// 256 + s*D (fp32 128xD).
+// 128x128), P (bf16 pairs) of warpgroup w at 256 + 64*w, O of row s at
+// 384 + s*D (fp32 128xD).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(384, 1)
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_q, bar_kv_full[C::NS], bar_kv_empty[C::NS], bar_bias_full[2],
       bar_bias_empty[2], bar_raw, bar_raw_free, bar_s_full[2], bar_s_free[2], bar_p_ready[2], bar_p_free[2],
-      bar_o_done[C::G], bar_drain;
+      bar_o_done[C::G], bar_drain[2];
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
 
@@ -121,10 +124,10 @@ __global__ void __launch_bounds__(384, 1)
     abort_flag = 0;
     mbar_init(&bar_q, 1);
     mbar_init(&bar_raw, 1);
-    mbar_init(&bar_raw_free, 2);  // both transposing warps
+    mbar_init(&bar_raw_free, 1);  // the transposing warp
     for (int i = 0; i < C::NS; ++i) { mbar_init(&bar_kv_full[i], 1); mbar_init(&bar_kv_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_bias_full[i], BIAS_K_CONTIG ? 1 : 2);
+      mbar_init(&bar_bias_full[i], 1);
       mbar_init(&bar_bias_empty[i], 128 * n_wg);
       mbar_init(&bar_s_full[i], 1);
       mbar_init(&bar_s_free[i], 128);
@@ -132,7 +135,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bar_p_free[i], 1);
     }
     for (int i = 0; i < C::G; ++i) mbar_init(&bar_o_done[i], 1);
-    mbar_init(&bar_drain, 1);
+    mbar_init(&bar_drain[0], 1);
+    mbar_init(&bar_drain[1], 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(&tmem_base_slot, C::TMEM_COLS);
@@ -279,99 +283,89 @@ __global__ void __launch_bounds__(384, 1)
       mbar_wait(&bar_q, 0, &no_abort);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // =================== MMA issuer ========================================
+  } else if (warp <= 2) {
+    // =================== MMA issuers (warp 1: warpgroup 0, warp 2: 1) ======
+    const int w = warp - 1;
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q, K both K-major
       constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);    // P from TMEM, V MN-major
-      // A single thread issues every MMA, so its own instruction latency
-      // paces the tensor core: descriptors are built once and offset by
-      // constants, and tile bookkeeping uses additions only.
+      // The issuing thread's own instruction latency paces small MMAs:
+      // descriptors are built once and offset by constants, and the tile
+      // bookkeeping uses additions only.
       const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
       const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
       const uint64_t dv0 = umma_desc(smem_u32(smem + C::OFF_V), 16, C::ATOM, C::SW);
       bool ok = mbar_wait(&bar_q, 0, wctx);
-      // Poll: for each warpgroup independently, issue S = QK^T of its next
-      // tile as soon as that tile's K/V stage is loaded and the warpgroup has
-      // taken its previous S into registers, and O += PV of its oldest tile
-      // as soon as that P is stored; neither warpgroup waits for the other.
-      // A cursor walks the tiles (kt, s) of one warpgroup: s = w, w+2, ...
+      // Poll: issue S = QK^T of this warpgroup's next tile as soon as its K/V
+      // stage is loaded and the warpgroup has taken its previous S into
+      // registers, and O += PV of its oldest tile as soon as that P is
+      // stored.  A cursor walks the tiles (kt, s) of the warpgroup:
+      // s = w, w+2, ...
       struct Cur { int a, kt, s; };
-      auto advance = [&](Cur& c, int w) {
+      auto advance = [&](Cur& c) {
         c.s += 2;
         if (c.s >= g_eff) { c.s = w; ++c.kt; }
         c.a = c.kt * g_eff + c.s;
       };
-      Cur qc[2], pc[2];
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        qc[w] = Cur{w, w < g_eff ? 0 : nkt, w};
-        pc[w] = qc[w];
-      }
-      int n_qk[2] = {0, 0}, n_pv[2] = {0, 0};  // per-warpgroup counts issued
-      int pv_done = 0;
+      Cur qc{w, w < g_eff ? 0 : nkt, w};
+      Cur pc = qc;
+      const int my_total = w < g_eff ? nkt * ((g_eff - w + 1) / 2) : 0;
+      int n_qk = 0, n_pv = 0;
       Watchdog wd;
       wd.reset();
-      while (ok && pv_done < total) {
+      while (ok && n_pv < my_total) {
         bool prog = false;
-#pragma unroll
-        for (int w = 0; w < 2; ++w) {
-          Cur& c = qc[w];
-          if (c.kt < nkt) {
-            const int st = c.a % C::NS;
-            if ((n_qk[w] == 0 || mbar_test(&bar_s_free[w], (n_qk[w] - 1) & 1)) &&
-                mbar_test(&bar_kv_full[st], (c.a / C::NS) & 1)) {
-              tc_fence_after();
-              const uint64_t dq = dq0 + ((uint32_t)(c.s * C::TILE) >> 4);
-              const uint64_t dk = dk0 + ((uint32_t)(st * C::TILE) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk)
-                umma_ss(tmem + 128 * w, dq + 2 * kk, dk + 2 * kk, id_s, kk > 0);
-              umma_commit(&bar_s_full[w]);
-              ++n_qk[w];
-              advance(c, w);
-              prog = true;
-            }
-          }
-          Cur& e = pc[w];
-          if (e.kt < nkt && n_pv[w] < n_qk[w] && mbar_test(&bar_p_ready[w], n_pv[w] & 1)) {
-            const int st = e.a % C::NS;
+        if (qc.kt < nkt) {
+          const int st = qc.a % C::NS;
+          if ((n_qk == 0 || mbar_test(&bar_s_free[w], (n_qk - 1) & 1)) &&
+              mbar_test(&bar_kv_full[st], (qc.a / C::NS) & 1)) {
             tc_fence_after();
-            const uint64_t dv = dv0 + ((uint32_t)(st * C::TILE) >> 4);
-            const uint32_t o = tmem + C::TMEM_O + e.s * D, pa = tmem + C::TMEM_P + 64 * w;
+            const uint64_t dq = dq0 + ((uint32_t)(qc.s * C::TILE) >> 4);
+            const uint64_t dk = dk0 + ((uint32_t)(st * C::TILE) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_ts(o, pa + kk * 8, dv + kk * (16 * C::ROW >> 4), id_o, (e.kt > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&bar_kv_empty[st]);
-            umma_commit(&bar_o_done[e.s]);
-            umma_commit(&bar_p_free[w]);
-            ++n_pv[w];
-            ++pv_done;
-            advance(e, w);
+            for (int kk = 0; kk < D / 16; ++kk)
+              umma_ss(tmem + 128 * w, dq + 2 * kk, dk + 2 * kk, id_s, kk > 0);
+            umma_commit(&bar_s_full[w]);
+            ++n_qk;
+            advance(qc);
             prog = true;
           }
+        }
+        if (n_pv < n_qk && mbar_test(&bar_p_ready[w], n_pv & 1)) {
+          const int st = pc.a % C::NS;
+          tc_fence_after();
+          const uint64_t dv = dv0 + ((uint32_t)(st * C::TILE) >> 4);
+          const uint32_t o = tmem + C::TMEM_O + pc.s * D, pa = tmem + C::TMEM_P + 64 * w;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(o, pa + kk * 8, dv + kk * (16 * C::ROW >> 4), id_o,
+                    (pc.kt > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&bar_kv_empty[st]);
+          umma_commit(&bar_o_done[pc.s]);
+          umma_commit(&bar_p_free[w]);
+          ++n_pv;
+          advance(pc);
+          prog = true;
         }
         if (prog) wd.reset();
         else if (!wd.poll(wctx)) ok = false;
       }
       // every issued MMA completes before TMEM can be released
-      umma_commit(&bar_drain);
+      umma_commit(&bar_drain[w]);
       volatile int no_abort = 0;
-      mbar_wait(&bar_drain, 0, &no_abort);
+      mbar_wait(&bar_drain[w], 0, &no_abort);
     }
     __syncwarp();
   }
   else if (!BIAS_K_CONTIG) {
-    // =================== bias transpose (warps 2-3) =========================
-    const int half = warp - 2;  // each warp moves 128 of the 256 8x8 blocks
+    // =================== bias transpose (warp 3) ============================
     for (int kt = 0; kt < nkt; ++kt) {
       const int bs = kt & 1;
       bool ok = true;
       if (kt >= 2) ok = mbar_wait(&bar_bias_empty[bs], ((kt >> 1) - 1) & 1, wctx);
       ok = ok && mbar_wait(&bar_raw, kt & 1, wctx);
       if (!__all_sync(0xffffffffu, ok)) break;
-      transpose_tile128_bf16(smem + C::OFF_RAW, smem + C::OFF_BIAS + bs * C::BIAS_TILE, lane,
-                             128 * half, 128);
+      transpose_tile128_bf16(smem + C::OFF_RAW, smem + C::OFF_BIAS + bs * C::BIAS_TILE, lane);
       fence_proxy_async_smem();  // generic reads of the staging buffer before its next TMA
       __syncwarp();
       if (lane == 0) {
