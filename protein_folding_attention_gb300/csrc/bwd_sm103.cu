@@ -433,13 +433,14 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ============================ MMA issuer ===============================
-    if (lane == 0) {
+    // The whole warp runs the loop (descriptors and bookkeeping stay
+    // warp-uniform); the elected lane issues each tcgen05.mma and commit.  A
+    // completed phase stays complete until this warp issues the work that
+    // feeds the next one, so any lane's observation of it holds for the warp.
+    {
       constexpr uint32_t id_sdp = idesc_bf16(128, 128, 0, 0);  // A=K/V, B=Q/dOa, K-major
       constexpr uint32_t id_kv = idesc_bf16(128, D, 0, 1);     // A=P^T/dS^T (TMEM), B MN-major
       constexpr uint32_t id_q = idesc_bf16(128, D, 1, 1);      // A=dS (smem, MN-major)
-      // A single thread issues every MMA, so its own instruction latency
-      // paces the tensor core: descriptors are built once and offset by
-      // constants, and tile bookkeeping uses additions only.
       const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
       const uint64_t dv0 = umma_desc(smem_u32(smem + C::OFF_V), 16, C::ATOM, C::SW);
       const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
@@ -456,7 +457,6 @@ __global__ void __launch_bounds__(384, 1)
       Cur ca{0, 0, 0, 0, 0}, cb{0, 0, 0, 0, 0};  // next S/dP tile, next dV/dK/dQ tile
       Watchdog wd;
       wd.reset();
-      bool ok = true;
       while (cb.t < total) {
         bool prog = false;
         // S/dP of tile t+1 go out as soon as the compute threads hold S/dP of
@@ -464,27 +464,30 @@ __global__ void __launch_bounds__(384, 1)
         // them while tile t's softmax runs (Q/dO stages: t, t+1 and t+2 live)
         if (ca.t < total && ca.t <= cb.t + 2) {
           const int kvs = ca.n & 1;
-          if ((ca.t == 0 || mbar_test(&bar_sdp_free, (ca.t - 1) & 1)) &&
-              mbar_test(&bar_qd_full[ca.qs], ca.qph) &&
-              (ca.jt != 0 || mbar_test(&bar_kv_full[kvs], (ca.n >> 1) & 1))) {
+          const bool ready = (ca.t == 0 || mbar_test(&bar_sdp_free, (ca.t - 1) & 1)) &&
+                             mbar_test(&bar_qd_full[ca.qs], ca.qph) &&
+                             (ca.jt != 0 || mbar_test(&bar_kv_full[kvs], (ca.n >> 1) & 1));
+          if (__any_sync(0xffffffffu, ready)) {
             tc_fence_after();
             const uint64_t dk = dk0 + kvs * TILE16, dv = dv0 + kvs * TILE16;
             const uint64_t dq = dq0 + ca.qs * TILE16, ddo = ddo0 + ca.qs * TILE16;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              umma_ss(tmem + C::T_S, dk + 2 * kk, dq + 2 * kk, id_sdp, kk > 0);
-              umma_ss(tmem + C::T_DP, dv + 2 * kk, ddo + 2 * kk, id_sdp, kk > 0);
+              if (elect_one()) umma_ss(tmem + C::T_S, dk + 2 * kk, dq + 2 * kk, id_sdp, kk > 0);
+              if (elect_one()) umma_ss(tmem + C::T_DP, dv + 2 * kk, ddo + 2 * kk, id_sdp, kk > 0);
             }
-            umma_commit(&bar_s_full);
+            if (elect_one()) umma_commit(&bar_s_full);
+            __syncwarp();
             advance(ca);
             prog = true;
           }
         }
         if (cb.t < ca.t) {
           const int kvs = cb.n & 1, bq = cb.t;
-          if (mbar_test(&bar_p_ready, bq & 1) &&
+          const bool ready = mbar_test(&bar_p_ready, bq & 1) &&
               (bq < 2 || mbar_test(&bar_dq_free[bq & 1], ((bq >> 1) - 1) & 1)) &&
-              (cb.jt != 0 || cb.n == 0 || mbar_test(&bar_dkdv_free, (cb.n - 1) & 1))) {
+              (cb.jt != 0 || cb.n == 0 || mbar_test(&bar_dkdv_free, (cb.n - 1) & 1));
+          if (__any_sync(0xffffffffu, ready)) {
             tc_fence_after();
             const uint64_t dq = dq0 + cb.qs * TILE16, ddo = ddo0 + cb.qs * TILE16;
             const uint64_t dk = dk0 + kvs * TILE16;
@@ -492,31 +495,37 @@ __global__ void __launch_bounds__(384, 1)
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t acc = (cb.jt > 0 || kk > 0) ? 1u : 0u;
               // dV += P^T dOa ; dK += dS^T Q  (K dimension = queries, 16 per step)
-              umma_ts(tmem + C::T_DV, tmem + C::T_P + kk * 8, ddo + kk * KSTEP16, id_kv, acc);
-              umma_ts(tmem + C::T_DK, tmem + C::T_DS + kk * 8, dq + kk * KSTEP16, id_kv, acc);
+              if (elect_one())
+                umma_ts(tmem + C::T_DV, tmem + C::T_P + kk * 8, ddo + kk * KSTEP16, id_kv, acc);
+              if (elect_one())
+                umma_ts(tmem + C::T_DK, tmem + C::T_DS + kk * 8, dq + kk * KSTEP16, id_kv, acc);
             }
             const uint32_t dqt = tmem + C::T_DQ + (bq & 1) * D;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K dimension = keys)
-              umma_ss(dqt, dds0 + kk * (2048 >> 4), dk + kk * KSTEP16, id_q, kk > 0);
-            umma_commit(&bar_qd_empty[cb.qs]);
-            if (cb.jt == njt - 1) umma_commit(&bar_kv_empty[kvs]);
-            umma_commit(&bar_mma_done);
+              if (elect_one()) umma_ss(dqt, dds0 + kk * (2048 >> 4), dk + kk * KSTEP16, id_q, kk > 0);
+            if (elect_one()) {
+              umma_commit(&bar_qd_empty[cb.qs]);
+              if (cb.jt == njt - 1) umma_commit(&bar_kv_empty[kvs]);
+              umma_commit(&bar_mma_done);
+            }
+            __syncwarp();
             advance(cb);
             prog = true;
           }
         }
         if (prog) {
           wd.reset();
-        } else if (!wd.poll(wctx)) {
-          ok = false;
+        } else if (!__all_sync(0xffffffffu, wd.poll(wctx))) {
           break;
         }
       }
-      (void)ok;
-      umma_commit(&bar_drain);
-      volatile int no_abort = 0;
-      mbar_wait(&bar_drain, 0, &no_abort);
+      if (elect_one()) umma_commit(&bar_drain);
+      __syncwarp();
+      if (lane == 0) {
+        volatile int no_abort = 0;
+        mbar_wait(&bar_drain, 0, &no_abort);
+      }
     }
     __syncwarp();
   }
@@ -852,7 +861,8 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ============================ MMA issuer ===============================
-    if (lane == 0) {
+    // whole warp, elected lane issues (as in the dK/dV kernel)
+    {
       constexpr uint32_t id = idesc_bf16(128, 128, 0, 0);
       const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
       const uint64_t ddo0 = umma_desc(smem_u32(smem + C::OFF_DO), 16, C::ATOM, C::SW);
@@ -863,20 +873,27 @@ __global__ void __launch_bounds__(384, 1)
         const int st = i % C::NST;
         ok = mbar_wait(&bar_full[st], (i / C::NST) & 1, wctx);
         if (ok && i > 0) ok = mbar_wait(&bar_sdp_free, (i - 1) & 1, wctx);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
         const uint32_t off = (uint32_t)(st * C::TILE) >> 4;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          umma_ss(tmem + C::T_S, dq0 + off + 2 * kk, dk0 + off + 2 * kk, id, kk > 0);
-          umma_ss(tmem + C::T_DP, ddo0 + off + 2 * kk, dv0 + off + 2 * kk, id, kk > 0);
+          if (elect_one()) umma_ss(tmem + C::T_S, dq0 + off + 2 * kk, dk0 + off + 2 * kk, id, kk > 0);
+          if (elect_one()) umma_ss(tmem + C::T_DP, ddo0 + off + 2 * kk, dv0 + off + 2 * kk, id, kk > 0);
         }
-        umma_commit(&bar_empty[st]);
-        umma_commit(&bar_s_full);
+        if (elect_one()) {
+          umma_commit(&bar_empty[st]);
+          umma_commit(&bar_s_full);
+        }
+        __syncwarp();
       }
-      umma_commit(&bar_drain);
-      volatile int no_abort = 0;
-      mbar_wait(&bar_drain, 0, &no_abort);
+      if (elect_one()) umma_commit(&bar_drain);
+      __syncwarp();
+      if (lane == 0) {
+        volatile int no_abort = 0;
+        mbar_wait(&bar_drain, 0, &no_abort);
+      }
     }
     __syncwarp();
   }

@@ -11,24 +11,37 @@
 // The key tiles kt form the outer loop and the G rows the inner loop, so each
 // 128x128 pair-bias tile is loaded into shared memory once and serves G rows.
 //
+// The pair bias is added by the tensor core.  Each logit tile accumulates
+//   T = Q K^T + (c I) * bias,      c = sqrt(D) rounded to bf16,
+// in tensor memory (I the 128x128 identity, so the second product has one
+// nonzero term per sum and adds c * bias[j, k] exactly in fp32); the softmax
+// then works on T / sqrt(D).  c is exact for D = 16 and 64; for D = 32 it is
+// 5.65625 against sqrt(32) = 5.656854, a relative error of 1.1e-4 in the bias
+// coefficient, twenty times below the bf16 rounding that P gets before the
+// PV product.  The identity is never stored whole: reduction chunk kk (bias
+// rows j' in [16kk, 16kk+16)) is the 128-row window, starting at row
+// 112 - 16kk, of a 240 x 16 matrix Z whose only nonzeros are Z[112 + i][i] =
+// c.  The MMA reads the bias tile in the layout the TMA delivers it: keys
+// contiguous (starting node, MSA) as an MN-major operand, queries contiguous
+// (the ending-node view) as a K-major operand, so neither is transposed.
+//
 // Warp roles (384 threads, three warpgroups):
-//   warp 0      TMA producer: Q tiles, the bias tile of each kt, K/V tiles of
-//               each (kt, s) and the additive key mask of that (s, kt)
-//   warps 1-2   MMA issuers, one thread each, warp 1 for softmax warpgroup 0
-//               and warp 2 for warpgroup 1: S = Q K^T into TMEM, O += P V
-//               with P read from TMEM.  An issuing thread spends ~50 cycles
-//               per tcgen05.mma, longer than an N = 32 MMA runs on the tensor
-//               core, so two issuers keep it fed
-//   warp 3      transposes a key-row-major (query-contiguous) bias tile into
-//               query rows; idle otherwise
+//   warp 0      TMA producer: Q tiles, K/V tiles of each (kt, s) and the
+//               additive key mask of that (s, kt)
+//   warps 1-2   MMA issuers of softmax warpgroups 0 and 1: T per tile, then
+//               O += P V with P read from tensor memory
+//   warp 3      TMA producer of the bias tile of each kt
 //   warps 4-7   softmax warpgroup 0: rows s = 0, 2, ... of the group
 //   warps 8-11  softmax warpgroup 1: rows s = 1, 3, ...
 // A softmax thread owns one query row j (TMEM lane 32*(warp%4) + lane).
 //
-// Tensor memory (512 columns): S buffer of warpgroup w at columns 128*w (fp32
-// 128x128), P (bf16 pairs) of warpgroup w at 256 + 64*w, O of row s at
-// 384 + s*D (fp32 128xD).
+// Tensor memory (512 columns): three T buffers at 0, 128, 256 (fp32
+// 128x128), used by tile i = kt*G + s in turn (buffer i % 3); the bf16 P of a
+// tile overwrites the first 64 columns of its buffer.  O of row s at 384 +
+// s*D (fp32 128xD).  With three buffers the T of a warpgroup's next tile is
+// computed while the warpgroup still works on its current one.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -48,33 +61,34 @@ struct FwdCfg {
   static constexpr int BM = 128;                   // query rows per tile
   static constexpr int BN = 128;                   // keys per tile
   static constexpr int G = (D == 64) ? 2 : 4;      // rows s per CTA
-  static constexpr int NS = (D == 64) ? 3 : 4;     // K/V pipeline stages
+  static constexpr int NS = (D == 64) ? 3 : 5;     // K/V pipeline stages
+  static constexpr int NT = 3;                     // T buffers in tensor memory
   static constexpr uint32_t ROW = D * 2;           // bytes of one bf16 row
   static constexpr uint32_t ATOM = 8 * ROW;        // swizzle atom (8 rows)
   static constexpr Swizzle SW = D == 16 ? kSw32 : (D == 32 ? kSw64 : kSw128);
   static constexpr uint32_t TILE = 128 * ROW;      // one 128-row Q/K/V tile
   static constexpr uint32_t BIAS_TILE = 128 * 128 * 2;
+  static constexpr uint32_t Z_BYTES = 240 * 32;    // identity windows, 32-byte rows
   // shared memory carve-up (offsets from a 1024-aligned base)
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + G * TILE;
   static constexpr uint32_t OFF_V = OFF_K + NS * TILE;
-  static constexpr uint32_t OFF_BIAS = OFF_V + NS * TILE;       // 2 stages, rows = query j
-  static constexpr uint32_t OFF_RAW = OFF_BIAS + 2 * BIAS_TILE; // staging of a j-contiguous bias
-  static constexpr uint32_t OFF_MADD = OFF_RAW + BIAS_TILE;
+  static constexpr uint32_t OFF_BIAS = OFF_V + NS * TILE;       // 2 stages
+  static constexpr uint32_t OFF_Z = OFF_BIAS + 2 * BIAS_TILE;
+  static constexpr uint32_t OFF_MADD = OFF_Z + Z_BYTES;
   static constexpr uint32_t OFF_FLAG = OFF_MADD + NS * BN * 4;  // per stage: tile has masked keys
   static constexpr uint32_t SMEM = OFF_FLAG + NS * 16;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
-  // tensor memory: S of warpgroup w at 128*w, P of warpgroup w at 256 + 64*w,
-  // O of row s at 384 + s*D
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t TMEM_P = 256;
   static constexpr uint32_t TMEM_O = 384;
   static constexpr int THREADS = 384;
   // register split: launch 168/thread; the producer warpgroup drops to 80,
   // the softmax warpgroups rise to 208 (80*128 + 208*256 <= 168*384)
   static constexpr int LAUNCH_REGS = 168, REGS_LOW = 80, REGS_HIGH = 208;
   static_assert(REGS_LOW * 128 + REGS_HIGH * 256 <= LAUNCH_REGS * THREADS, "register split");
-  static_assert(TMEM_O + G * D <= TMEM_COLS, "tensor memory overflow");
+  static_assert(NT * 128 <= TMEM_O && TMEM_O + G * D <= TMEM_COLS, "tensor memory overflow");
+  static_assert(OFF_BIAS % 1024 == 0 && OFF_Z % 256 == 0, "operand alignment");
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory");
 };
 
 struct FwdParams {
@@ -101,8 +115,8 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_q, bar_kv_full[C::NS], bar_kv_empty[C::NS], bar_bias_full[2],
-      bar_bias_empty[2], bar_raw, bar_raw_free, bar_s_full[2], bar_s_free[2], bar_p_ready[2], bar_p_free[2],
-      bar_o_done[C::G], bar_drain[2];
+      bar_bias_empty[2], bar_s_full[2], bar_s_free[C::NT], bar_p_ready[2], bar_o_done[C::G],
+      bar_drain[2];
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
 
@@ -123,21 +137,30 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_q, 1);
-    mbar_init(&bar_raw, 1);
-    mbar_init(&bar_raw_free, 1);  // the transposing warp
     for (int i = 0; i < C::NS; ++i) { mbar_init(&bar_kv_full[i], 1); mbar_init(&bar_kv_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_bias_full[i], 1);
-      mbar_init(&bar_bias_empty[i], 128 * n_wg);
+      mbar_init(&bar_bias_empty[i], n_wg);  // each active issuer, after its last tile of a kt
       mbar_init(&bar_s_full[i], 1);
-      mbar_init(&bar_s_free[i], 128);
       mbar_init(&bar_p_ready[i], 128);
-      mbar_init(&bar_p_free[i], 1);
+      mbar_init(&bar_drain[i], 1);
     }
+    for (int i = 0; i < C::NT; ++i) mbar_init(&bar_s_free[i], 1);
     for (int i = 0; i < C::G; ++i) mbar_init(&bar_o_done[i], 1);
-    mbar_init(&bar_drain[0], 1);
-    mbar_init(&bar_drain[1], 1);
     fence_barrier_init();
+  }
+  // Z in the 32-byte-swizzled K-major layout the MMA reads: row r holds 16
+  // bf16 values in two 16-byte chunks, stored swapped when bit 2 of r is set.
+  {
+    const uint32_t cb = __bfloat16_as_ushort(__float2bfloat16_rn(sqrtf((float)D)));
+    uint32_t* z32 = reinterpret_cast<uint32_t*>(smem + C::OFF_Z);
+    for (int i = threadIdx.x; i < (int)(C::Z_BYTES / 4); i += C::THREADS) {
+      const int r = i >> 3, wd = i & 7;
+      const int c0 = (((wd >> 2) ^ ((r >> 2) & 1)) << 3) + ((wd & 3) << 1);
+      const int one = r - 112;  // column of this row's nonzero, if any
+      z32[i] = one == c0 ? cb : (one == c0 + 1 ? cb << 16 : 0u);
+    }
+    fence_proxy_async_smem();  // generic writes, read by the tensor core
   }
   if (warp == 1) tmem_alloc(&tmem_base_slot, C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
@@ -162,44 +185,24 @@ __global__ void __launch_bounds__(384, 1)
     }
     if (threadIdx.x == 0) report_abort(abort_p, p.status);
   };
-
   if (warp < 4) {
   // setmaxnreg is warpgroup-aligned: one instance for warps 0-3, one for 4-11
   regs_dec<C::REGS_LOW>();
   if (warp == 0) {
     // =================== TMA producer (whole warp) ========================
-    // A query-row-major bias tile ([j][k], keys contiguous) goes straight to
-    // its stage; a key-row-major one (the ending-node view) lands in a
-    // staging buffer and the warp transposes it into the stage.
     // The copy engine serves the copies one thread issues in order, but
     // those of different threads concurrently; with 64-byte rows a single
     // issuing thread would cap the loads at ~10 bytes/clock.  Each box is
     // therefore issued by the next lane of the warp in turn (the whole warp
     // calls these helpers; lane 0 arms the barrier first).
     int rr = 0;
-    auto issue_bias = [&](int kt, uint8_t* dst, uint64_t* bar) {
-      if (lane == 0) mbar_arrive_expect_tx(bar, C::BIAS_TILE);
-      __syncwarp();
-      const int l0 = rr & 31, l1 = (rr + 1) & 31;
-      rr += 2;
-      if (BIAS_K_CONTIG) {
-        if (lane == l0) tma_load_4d(dst, &tm_bias, bar, kt * C::BN, jt * C::BM, h, b);
-        if (lane == l1)
-          tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, bar, kt * C::BN + 64, jt * C::BM, h, b);
-      } else {
-        if (lane == l0) tma_load_4d(dst, &tm_bias, bar, jt * C::BM, kt * C::BN, h, b);
-        if (lane == l1)
-          tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, bar, jt * C::BM + 64, kt * C::BN, h, b);
-      }
-    };
     if (lane == 0) mbar_arrive_expect_tx(&bar_q, g_eff * C::TILE);
     __syncwarp();
     if (lane < g_eff)
       tma_load_5d(smem + C::OFF_Q + lane * C::TILE, &tm_q, &bar_q, 0, jt * C::BM, h, s0 + lane, b);
     rr = g_eff;
-    if (!BIAS_K_CONTIG) issue_bias(0, smem + C::OFF_RAW, &bar_raw);
     bool ok = true;
-    int kv_issued = 0, bias_issued = 0, raw_issued = BIAS_K_CONTIG ? 0 : 1;
+    int kv_issued = 0;
     // mask bytes of the next (kt, s) are loaded while the current is armed
     unsigned char pre_m[4];
     auto prefetch_mask = [&](int i) {
@@ -214,24 +217,15 @@ __global__ void __launch_bounds__(384, 1)
     };
     prefetch_mask(0);
     for (int kt = 0; kt < nkt && ok; ++kt) {
-      const int bs = kt & 1;
-      uint8_t* stage = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
-      if (BIAS_K_CONTIG && kt >= 2) ok = mbar_wait(&bar_bias_empty[bs], ((kt >> 1) - 1) & 1, wctx);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      if (BIAS_K_CONTIG) {
-        issue_bias(kt, stage, &bar_bias_full[bs]);
-      }
-      bias_issued = kt + 1;
       for (int s = 0; s < g_eff; ++s) {
         const int i = kt * g_eff + s;
         const int st = i % C::NS;
         if (i >= C::NS) ok = mbar_wait(&bar_kv_empty[st], ((i / C::NS) - 1) & 1, wctx);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        // additive key mask of (s, kt) in units of the unscaled logit
-        // (S + sqrt(D) bias): 0 kept, -1e9*sqrt(D) masked, -inf beyond N; and a
-        // flag telling the softmax whether the tile has any such key
+        // additive key mask of (s, kt) in units of T (logit * sqrt(D)): 0
+        // kept, -1e9*sqrt(D) masked, -inf beyond N; and a flag telling the
+        // softmax whether the tile has any such key
         float* madd = reinterpret_cast<float*>(smem + C::OFF_MADD + st * C::BN * 4);
         bool any = false;
 #pragma unroll
@@ -258,14 +252,6 @@ __global__ void __launch_bounds__(384, 1)
         rr += 2;
         kv_issued = i + 1;
       }
-      if (!ok) break;
-      if (!BIAS_K_CONTIG && kt + 1 < nkt) {
-        // the staging buffer is free once the transposing warps read tile kt
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw_free, kt & 1, wctx));
-        if (!ok) break;
-        issue_bias(kt + 1, smem + C::OFF_RAW, &bar_raw);
-        raw_issued = kt + 2;
-      }
     }
     // After a give-up, let every copy already issued land before the CTA may
     // exit (those waits end by themselves: a copy does not depend on the
@@ -274,105 +260,149 @@ __global__ void __launch_bounds__(384, 1)
       volatile int no_abort = 0;
       for (int i = max(0, kv_issued - C::NS); i < kv_issued; ++i)
         mbar_wait(&bar_kv_full[i % C::NS], (i / C::NS) & 1, &no_abort);
-      if (BIAS_K_CONTIG) {
-        for (int kt = max(0, bias_issued - 2); kt < bias_issued; ++kt)
-          mbar_wait(&bar_bias_full[kt & 1], (kt >> 1) & 1, &no_abort);
-      } else if (raw_issued > 0) {
-        mbar_wait(&bar_raw, (raw_issued - 1) & 1, &no_abort);
-      }
       mbar_wait(&bar_q, 0, &no_abort);
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // =================== TMA producer of the bias tiles (one lane) =========
+    // Its own warp, so that the K/V stream never waits for a bias stage.  A
+    // stage is free once the MMAs of every row of kt - 2 have read it.
+    if (lane == 0) {
+      bool ok = true;
+      int issued = 0;
+      for (int kt = 0; kt < nkt && ok; ++kt) {
+        const int bs = kt & 1;
+        if (kt >= 2) ok = mbar_wait(&bar_bias_empty[bs], ((kt >> 1) - 1) & 1, wctx);
+        if (!ok) break;
+        uint8_t* dst = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
+        mbar_arrive_expect_tx(&bar_bias_full[bs], C::BIAS_TILE);
+        if (BIAS_K_CONTIG) {  // rows j, keys contiguous
+          tma_load_4d(dst, &tm_bias, &bar_bias_full[bs], kt * C::BN, jt * C::BM, h, b);
+          tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, &bar_bias_full[bs], kt * C::BN + 64,
+                      jt * C::BM, h, b);
+        } else {              // rows k, queries contiguous
+          tma_load_4d(dst, &tm_bias, &bar_bias_full[bs], jt * C::BM, kt * C::BN, h, b);
+          tma_load_4d(dst + C::BIAS_TILE / 2, &tm_bias, &bar_bias_full[bs], jt * C::BM + 64,
+                      kt * C::BN, h, b);
+        }
+        issued = kt + 1;
+      }
+      if (!ok) {  // let the copies already issued land
+        volatile int no_abort = 0;
+        for (int kt = max(0, issued - 2); kt < issued; ++kt)
+          mbar_wait(&bar_bias_full[kt & 1], (kt >> 1) & 1, &no_abort);
+      }
     }
     __syncwarp();
   } else if (warp <= 2) {
     // =================== MMA issuers (warp 1: warpgroup 0, warp 2: 1) ======
+    // Each waits (suspended in mbarrier.try_wait) for exactly the event its
+    // next MMA needs.  Order per warpgroup: T of its next tile goes out
+    // before O += P V of its current one, so the T buffer pool lets the
+    // tensor core compute a warpgroup's next logits while it still works on
+    // the current ones.  The whole warp runs the loop (descriptors stay
+    // warp-uniform); the elected lane, the same one throughout (the warp stays
+    // converged), issues each tcgen05.mma and commit.
     const int w = warp - 1;
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q, K both K-major
-      constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);    // P from TMEM, V MN-major
-      // The issuing thread's own instruction latency paces small MMAs:
-      // descriptors are built once and offset by constants, and the tile
-      // bookkeeping uses additions only.
-      const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
-      const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
-      const uint64_t dv0 = umma_desc(smem_u32(smem + C::OFF_V), 16, C::ATOM, C::SW);
-      bool ok = mbar_wait(&bar_q, 0, wctx);
-      // Poll: issue S = QK^T of this warpgroup's next tile as soon as its K/V
-      // stage is loaded and the warpgroup has taken its previous S into
-      // registers, and O += PV of its oldest tile as soon as that P is
-      // stored.  A cursor walks the tiles (kt, s) of the warpgroup:
-      // s = w, w+2, ...
-      struct Cur { int a, kt, s; };
-      auto advance = [&](Cur& c) {
-        c.s += 2;
-        if (c.s >= g_eff) { c.s = w; ++c.kt; }
-        c.a = c.kt * g_eff + c.s;
-      };
-      Cur qc{w, w < g_eff ? 0 : nkt, w};
-      Cur pc = qc;
-      const int my_total = w < g_eff ? nkt * ((g_eff - w + 1) / 2) : 0;
-      int n_qk = 0, n_pv = 0;
-      Watchdog wd;
-      wd.reset();
-      while (ok && n_pv < my_total) {
-        bool prog = false;
-        if (qc.kt < nkt) {
-          const int st = qc.a % C::NS;
-          if ((n_qk == 0 || mbar_test(&bar_s_free[w], (n_qk - 1) & 1)) &&
-              mbar_test(&bar_kv_full[st], (qc.a / C::NS) & 1)) {
-            tc_fence_after();
-            const uint64_t dq = dq0 + ((uint32_t)(qc.s * C::TILE) >> 4);
-            const uint64_t dk = dk0 + ((uint32_t)(st * C::TILE) >> 4);
+    constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q, K both K-major
+    constexpr uint32_t id_b = idesc_bf16(128, 128, 0, BIAS_K_CONTIG ? 1 : 0);
+    constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);    // P from TMEM, V MN-major
+    const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
+    const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
+    const uint64_t dv0 = umma_desc(smem_u32(smem + C::OFF_V), 16, C::ATOM, C::SW);
+    const uint64_t dz0 = umma_desc(smem_u32(smem + C::OFF_Z), 16, 256, kSw32);
+    // bias tile as the B operand (N = keys, K = queries j'): keys contiguous
+    // -> MN-major, 64-key halves 16 KB apart, 8 j'-rows per 1 KB; queries
+    // contiguous -> K-major rows of 64 j' per 128 B, halves 16 KB apart
+    const uint64_t dbias0 = BIAS_K_CONTIG
+                                ? umma_desc(smem_u32(smem + C::OFF_BIAS), 16384, 1024, kSw128)
+                                : umma_desc(smem_u32(smem + C::OFF_BIAS), 16, 1024, kSw128);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_q, 0, wctx));
+    const int s_last = w < g_eff ? w + 2 * ((g_eff - 1 - w) / 2) : -1;  // last own row of a kt
+    // cursor over this warpgroup's tiles (kt, s), s = w, w+2, ...
+    struct Cur { int kt, s, i; };
+    auto next = [&](Cur c) {
+      c.s += 2;
+      if (c.s >= g_eff) { c.s = w; ++c.kt; }
+      c.i = c.kt * g_eff + c.s;
+      return c;
+    };
+    auto issue_t = [&](const Cur& c) {
+      const int st = c.i % C::NS, buf = c.i % C::NT;
+      bool r = mbar_wait(&bar_kv_full[st], (c.i / C::NS) & 1, wctx);
+      if (r && c.i >= C::NT) r = mbar_wait(&bar_s_free[buf], ((c.i / C::NT) - 1) & 1, wctx);
+      if (r) r = mbar_wait(&bar_bias_full[c.kt & 1], (c.kt >> 1) & 1, wctx);
+      if (!__all_sync(0xffffffffu, r)) return false;
+      tc_fence_after();
+      const uint32_t tb = tmem + 128 * buf;
+      const uint64_t dq = dq0 + ((uint32_t)(c.s * C::TILE) >> 4);
+      const uint64_t dk = dk0 + ((uint32_t)(st * C::TILE) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              umma_ss(tmem + 128 * w, dq + 2 * kk, dk + 2 * kk, id_s, kk > 0);
-            umma_commit(&bar_s_full[w]);
-            ++n_qk;
-            advance(qc);
-            prog = true;
-          }
-        }
-        if (n_pv < n_qk && mbar_test(&bar_p_ready[w], n_pv & 1)) {
-          const int st = pc.a % C::NS;
-          tc_fence_after();
-          const uint64_t dv = dv0 + ((uint32_t)(st * C::TILE) >> 4);
-          const uint32_t o = tmem + C::TMEM_O + pc.s * D, pa = tmem + C::TMEM_P + 64 * w;
+      for (int kk = 0; kk < D / 16; ++kk)
+        if (elect_one()) umma_ss(tb, dq + 2 * kk, dk + 2 * kk, id_s, kk > 0);
+      const uint64_t db = dbias0 + ((uint32_t)((c.kt & 1) * C::BIAS_TILE) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ts(o, pa + kk * 8, dv + kk * (16 * C::ROW >> 4), id_o,
-                    (pc.kt > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&bar_kv_empty[st]);
-          umma_commit(&bar_o_done[pc.s]);
-          umma_commit(&bar_p_free[w]);
-          ++n_pv;
-          advance(pc);
-          prog = true;
-        }
-        if (prog) wd.reset();
-        else if (!wd.poll(wctx)) ok = false;
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t a = dz0 + ((uint32_t)((112 - 16 * kk) * 32) >> 4);
+        const uint64_t bb = BIAS_K_CONTIG
+                                ? db + ((uint32_t)(kk * 2048) >> 4)
+                                : db + ((uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+        if (elect_one()) umma_ss(tb, a, bb, id_b, 1u);
       }
-      // every issued MMA completes before TMEM can be released
-      umma_commit(&bar_drain[w]);
+      if (elect_one()) {
+        umma_commit(&bar_s_full[w]);
+        if (c.s == s_last) umma_commit(&bar_bias_empty[c.kt & 1]);
+      }
+      __syncwarp();
+      return true;
+    };
+    auto issue_pv = [&](const Cur& c, int n) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_p_ready[w], n & 1, wctx))) return false;
+      tc_fence_after();
+      const int st = c.i % C::NS, buf = c.i % C::NT;
+      const uint64_t dv = dv0 + ((uint32_t)(st * C::TILE) >> 4);
+      const uint32_t o = tmem + C::TMEM_O + c.s * D, pa = tmem + 128 * buf;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        if (elect_one())
+          umma_ts(o, pa + kk * 8, dv + kk * (16 * C::ROW >> 4), id_o,
+                  (c.kt > 0 || kk > 0) ? 1u : 0u);
+      if (elect_one()) {
+        umma_commit(&bar_kv_empty[st]);
+        umma_commit(&bar_o_done[c.s]);
+        umma_commit(&bar_s_free[buf]);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (w < g_eff) {
+      const int my_total = nkt * ((g_eff - w + 1) / 2);
+      Cur cur{0, w, w};
+      if (ok) ok = issue_t(cur);
+      for (int n = 0; n < my_total && ok; ++n) {
+        const Cur nx = next(cur);
+        if (n + 1 < my_total) {
+          // T of the next tile first, unless its buffer is the one whose P
+          // the current tile's PV still has to read
+          if (nx.i - C::NT == cur.i) {
+            ok = issue_pv(cur, n) && issue_t(nx);
+          } else {
+            ok = issue_t(nx) && issue_pv(cur, n);
+          }
+        } else {
+          ok = issue_pv(cur, n);
+        }
+        cur = nx;
+      }
+    }
+    // every issued MMA completes before TMEM can be released
+    if (elect_one()) umma_commit(&bar_drain[w]);
+    __syncwarp();
+    if (lane == 0) {
       volatile int no_abort = 0;
       mbar_wait(&bar_drain[w], 0, &no_abort);
     }
     __syncwarp();
-  }
-  else if (!BIAS_K_CONTIG) {
-    // =================== bias transpose (warp 3) ============================
-    for (int kt = 0; kt < nkt; ++kt) {
-      const int bs = kt & 1;
-      bool ok = true;
-      if (kt >= 2) ok = mbar_wait(&bar_bias_empty[bs], ((kt >> 1) - 1) & 1, wctx);
-      ok = ok && mbar_wait(&bar_raw, kt & 1, wctx);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      transpose_tile128_bf16(smem + C::OFF_RAW, smem + C::OFF_BIAS + bs * C::BIAS_TILE, lane);
-      fence_proxy_async_smem();  // generic reads of the staging buffer before its next TMA
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bar_raw_free);
-        mbar_arrive(&bar_bias_full[bs]);
-      }
-    }
   }
   teardown();
   } else {
@@ -383,74 +413,57 @@ __global__ void __launch_bounds__(384, 1)
     const int row = quad * 32 + lane;                // query row within the tile
     const int j = jt * C::BM + row;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-    const float c1 = kLog2e * rsqrtf((float)D);      // logit scale in log2 units
-    const float sqd = sqrtf((float)D);
-    const float2 c1c1 = make_float2(c1, c1), sqd2 = make_float2(sqd, sqd);
-    const float lazy_thr = 8.0f / c1;                // 8 in log2 units, in t' units
-    float m_run[C::G / 2], l_run[C::G / 2];  // running max (t' units) and sum
+    const float c1 = kLog2e / sqrtf((float)D);       // T to log2 units
+    const float2 c1c1 = make_float2(c1, c1);
+    const float lazy_thr = 8.0f / c1;                // 2^8 in probability, in T units
+    float m_run[C::G / 2], l_run[C::G / 2];          // running max (T units) and sum
 #pragma unroll
     for (int u = 0; u < C::G / 2; ++u) { m_run[u] = -INFINITY; l_run[u] = 0.f; }
     bool ok = wg < n_wg;
-    int it = 0;  // iterations done by this warpgroup
+    int it = 0;  // tiles done by this warpgroup
     for (int kt = 0; kt < nkt && ok; ++kt) {
-      const int bs = kt & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_bias_full[bs], (kt >> 1) & 1, wctx));
-      if (!ok) break;
-      const uint8_t* brow = smem + C::OFF_BIAS + bs * C::BIAS_TILE + row * 128;
 #pragma unroll
       for (int u = 0; u < C::G / 2; ++u) {
         const int s = 2 * u + wg;
         if (s >= g_eff) break;
         const int i = kt * g_eff + s;
         const int st = i % C::NS;
-        ok = mbar_wait(&bar_kv_full[st], (i / C::NS) & 1, wctx) &&
-             mbar_wait(&bar_s_full[wg], it & 1, wctx);
-        ok = __all_sync(0xffffffffu, ok);
+        const uint32_t tcol = lane_base + 128 * (i % C::NT);  // T of this tile, then P
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[wg], it & 1, wctx));
         if (!ok) break;
         tc_fence_after();
         uint32_t x[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          tmem_ld32(lane_base + 128 * wg + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+          tmem_ld32(tcol + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bar_s_free[wg]);  // S may now be overwritten by the next QK^T
-        const float* madd = reinterpret_cast<const float*>(smem + C::OFF_MADD + st * C::BN * 4);
-        const bool masked = *reinterpret_cast<const int*>(smem + C::OFF_FLAG + st * 16) != 0;
-        // t' = S + sqrt(D) * bias (+ mask), in place: the logit in log2 units is
-        // c1 * t'.  4 independent max chains.
+        // key mask (warp-uniform flag: most tiles have no masked key), then
+        // the row max over 4 independent chains
+        if (*reinterpret_cast<const int*>(smem + C::OFF_FLAG + st * 16) != 0) {
+          const float* madd = reinterpret_cast<const float*>(smem + C::OFF_MADD + st * C::BN * 4);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float4 m4 = *reinterpret_cast<const float4*>(madd + 4 * c);
+            const float2 a = add2(make_float2(__uint_as_float(x[4 * c]), __uint_as_float(x[4 * c + 1])),
+                                  make_float2(m4.x, m4.y));
+            const float2 bq = add2(make_float2(__uint_as_float(x[4 * c + 2]), __uint_as_float(x[4 * c + 3])),
+                                   make_float2(m4.z, m4.w));
+            x[4 * c] = __float_as_uint(a.x); x[4 * c + 1] = __float_as_uint(a.y);
+            x[4 * c + 2] = __float_as_uint(bq.x); x[4 * c + 3] = __float_as_uint(bq.y);
+          }
+        }
         float mx[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) mx[e] = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint4 w4 = *reinterpret_cast<const uint4*>(
-              brow + (c >> 3) * (C::BIAS_TILE / 2) + ((((c & 7) ^ (row & 7))) << 4));
-          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-          float2 mv[4];
-          if (masked) {  // warp-uniform
-            const float4 ma = *reinterpret_cast<const float4*>(madd + 8 * c);
-            const float4 mb = *reinterpret_cast<const float4*>(madd + 8 * c + 4);
-            mv[0] = make_float2(ma.x, ma.y); mv[1] = make_float2(ma.z, ma.w);
-            mv[2] = make_float2(mb.x, mb.y); mv[3] = make_float2(mb.z, mb.w);
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k2 = 8 * c + 2 * e;
-            float2 t = fma2(make_float2(bf16lo(wv[e]), bf16hi(wv[e])), sqd2,
-                            make_float2(__uint_as_float(x[k2]), __uint_as_float(x[k2 + 1])));
-            if (masked) t = add2(t, mv[e]);
-            x[k2] = __float_as_uint(t.x);
-            x[k2 + 1] = __float_as_uint(t.y);
-            mx[e] = fmax3(mx[e], t.x, t.y);
-          }
-        }
+        for (int k2 = 0; k2 < 128; k2 += 2)
+          mx[(k2 >> 1) & 3] = fmax3(mx[(k2 >> 1) & 3], __uint_as_float(x[k2]), __uint_as_float(x[k2 + 1]));
         const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         // The reference max m moves only when the tile's max exceeds it by
-        // more than 2^8 in probability (8 in log2 units): P then stays <= 256,
-        // exact in fp32 and at full relative precision in bf16, and most
-        // tiles skip the O rescale.  Any m gives the same softmax.
-        const float m_new = rmax > m_run[u] + lazy_thr ? rmax : m_run[u];  // t' units
+        // more than 2^8 in probability: P then stays <= 256, exact in fp32
+        // and at full relative precision in bf16, and most tiles skip the O
+        // rescale.  Any m gives the same softmax.
+        const float m_new = rmax > m_run[u] + lazy_thr ? rmax : m_run[u];
         const float alpha = ex2((m_run[u] - m_new) * c1);
         // rescale O of this row when its running max moved (warp-uniform)
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
@@ -467,12 +480,8 @@ __global__ void __launch_bounds__(384, 1)
             tmem_st16(lane_base + C::TMEM_O + s * D + 16 * c, o);
           }
         }
-        // P of the previous iteration has been consumed by its PV
-        if (it > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bar_p_free[wg], (it - 1) & 1, wctx));
-          if (!ok) break;
-          tc_fence_after();
-        }
+        // P = exp2(c1 (T - m)) as bf16 pairs over the first 64 columns of the
+        // tile's T buffer (all of T is in registers by now)
         const float2 negm = make_float2(-m_new * c1, -m_new * c1);
         float2 sum[4];
 #pragma unroll
@@ -489,7 +498,7 @@ __global__ void __launch_bounds__(384, 1)
             sum[e & 3] = add2(sum[e & 3], pr);
             pk[e] = pack_bf16(pr.x, pr.y);
           }
-          tmem_st16(lane_base + C::TMEM_P + 64 * wg + 16 * q4, pk);
+          tmem_st16(tcol + 16 * q4, pk);
         }
         const float2 s01 = add2(sum[0], sum[1]), s23 = add2(sum[2], sum[3]);
         l_run[u] = l_run[u] * alpha + ((s01.x + s01.y) + (s23.x + s23.y));
@@ -499,8 +508,6 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(&bar_p_ready[wg]);
         ++it;
       }
-      if (!ok) break;
-      mbar_arrive(&bar_bias_empty[bs]);
     }
     // ---- epilogue: O / l, sigmoid gate, lse -------------------------------
     if (ok) {
