@@ -183,17 +183,13 @@ __device__ __forceinline__ float bias_at(const uint8_t* tile, int j, int k) {
 // barrier phase continues from one item to the next and the producer runs
 // ahead into the next item (K/V are double-buffered per item).
 //
-// Warps (384 threads): 0 TMA producer, 1 MMA issuer, 2-3 idle (their
-// warpgroup hands registers to the compute warpgroups), 4-11 two compute
-// warpgroups.  A compute thread owns key k (TMEM lane 32*(warp%4)+lane) and,
+// Warps (384 threads): 0 TMA producer, 1-3 MMA issuers (S/dP, dV/dK, dQ),
+// 4-11 two compute warpgroups.  A compute thread owns key k (TMEM lane 32*(warp%4)+lane) and,
 // of each 128-query tile, the 64 queries of its warpgroup's half.  Tensor
 // memory columns: S^T 0..127, dP^T 128..255 (fp32, lane = key), P^T 256..,
 // dS^T 320.. (bf16 pairs, 32 columns per half), two dQ partial buffers
 // 384.. (lane = query), dK and dV after them (lane = key).
 //
-// The MMA thread polls its barriers (mbarrier.test_wait) and issues
-// whichever is ready of: S/dP of the next tile, and dV/dK/dQ of the oldest
-// tile whose P/dS are stored, so neither waits behind the other.
 template <int D, bool BIAS_K_CONTIG>
 struct DkdvCfg : Tile<D> {
   using T = Tile<D>;
@@ -248,7 +244,7 @@ __global__ void __launch_bounds__(384, 1)
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_kv_full[2], bar_kv_empty[2], bar_qd_full[C::NQ], bar_qd_empty[C::NQ],
       bar_b_full[C::NB], bar_b_empty[C::NB], bar_raw, bar_s_full, bar_sdp_free, bar_p_ready,
-      bar_mma_done, bar_dq_free[2], bar_dkdv_free, bar_drain;
+      bar_mma_done, bar_dq_free[2], bar_dkdv_free, bar_drain[3];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -279,7 +275,9 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < C::NB; ++i) { mbar_init(&bar_b_full[i], 1); mbar_init(&bar_b_empty[i], 256); }
     mbar_init(&bar_raw, 1);
     mbar_init(&bar_s_full, 1); mbar_init(&bar_sdp_free, 256); mbar_init(&bar_p_ready, 256);
-    mbar_init(&bar_mma_done, 1); mbar_init(&bar_dkdv_free, 256); mbar_init(&bar_drain, 1);
+    // dV/dK and dQ of a tile are committed by two issuers
+    mbar_init(&bar_mma_done, 2); mbar_init(&bar_dkdv_free, 256);
+    for (int i = 0; i < 3; ++i) mbar_init(&bar_drain[i], 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(&tmem_slot, 512);
@@ -431,105 +429,116 @@ __global__ void __launch_bounds__(384, 1)
       if (raw_issued > 0) mbar_wait(&bar_raw, (raw_issued - 1) & 1, &no_abort);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ============================ MMA issuer ===============================
-    // The whole warp runs the loop (descriptors and bookkeeping stay
-    // warp-uniform); the elected lane issues each tcgen05.mma and commit.  A
-    // completed phase stays complete until this warp issues the work that
-    // feeds the next one, so any lane's observation of it holds for the warp.
-    {
+  } else {
+    // ============================ MMA issuers ==============================
+    // Warp 1 issues S^T / dP^T, warp 2 dV and dK, warp 3 dQ.  Each waits
+    // (suspended in mbarrier.try_wait) for exactly what its next MMAs need,
+    // so the small N = D products of one tile go out from two threads at
+    // once and none of them waits behind another's dependencies.  The whole
+    // warp runs the loop (descriptors stay warp-uniform); the elected lane,
+    // the same one throughout, issues each tcgen05.mma and commit.
+    constexpr uint32_t TILE16 = C::TILE >> 4, KSTEP16 = (16 * C::ROW) >> 4;
+    bool ok = true;
+    if (warp == 1) {
+      // S^T = K Q^T and dP^T = V dOa^T once Q/dOa (and, on an item's first
+      // tile, K/V) are loaded and S/dP of the previous tile are in the
+      // compute threads' registers
       constexpr uint32_t id_sdp = idesc_bf16(128, 128, 0, 0);  // A=K/V, B=Q/dOa, K-major
-      constexpr uint32_t id_kv = idesc_bf16(128, D, 0, 1);     // A=P^T/dS^T (TMEM), B MN-major
-      constexpr uint32_t id_q = idesc_bf16(128, D, 1, 1);      // A=dS (smem, MN-major)
       const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
       const uint64_t dv0 = umma_desc(smem_u32(smem + C::OFF_V), 16, C::ATOM, C::SW);
       const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
       const uint64_t ddo0 = umma_desc(smem_u32(smem + C::OFF_DO), 16, C::ATOM, C::SW);
+      int g = 0;
+      for (int n = 0; n < my_items && ok; ++n) {
+        const int kvs = n & 1;
+        for (int jt = 0; jt < njt; ++jt, ++g) {
+          const int qs = g % C::NQ;
+          ok = mbar_wait(&bar_qd_full[qs], (g / C::NQ) & 1, wctx);
+          if (ok && jt == 0) ok = mbar_wait(&bar_kv_full[kvs], (n >> 1) & 1, wctx);
+          if (ok && g > 0) ok = mbar_wait(&bar_sdp_free, (g - 1) & 1, wctx);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t dk = dk0 + kvs * TILE16, dv = dv0 + kvs * TILE16;
+          const uint64_t dq = dq0 + qs * TILE16, ddo = ddo0 + qs * TILE16;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            if (elect_one()) umma_ss(tmem + C::T_S, dk + 2 * kk, dq + 2 * kk, id_sdp, kk > 0);
+            if (elect_one()) umma_ss(tmem + C::T_DP, dv + 2 * kk, ddo + 2 * kk, id_sdp, kk > 0);
+          }
+          if (elect_one()) umma_commit(&bar_s_full);
+          __syncwarp();
+        }
+      }
+    } else if (warp == 2) {
+      // dV += P^T dOa and dK += dS^T Q (K dimension = queries) once P^T and
+      // dS^T are stored; on an item's first tile the previous item's dK/dV
+      // must have been read out
+      constexpr uint32_t id_kv = idesc_bf16(128, D, 0, 1);  // A=P^T/dS^T (TMEM), B MN-major
+      const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
+      const uint64_t ddo0 = umma_desc(smem_u32(smem + C::OFF_DO), 16, C::ATOM, C::SW);
+      int g = 0;
+      for (int n = 0; n < my_items && ok; ++n) {
+        for (int jt = 0; jt < njt; ++jt, ++g) {
+          const int qs = g % C::NQ;
+          ok = mbar_wait(&bar_p_ready, g & 1, wctx);
+          if (ok && jt == 0 && n > 0) ok = mbar_wait(&bar_dkdv_free, (n - 1) & 1, wctx);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t dq = dq0 + qs * TILE16, ddo = ddo0 + qs * TILE16;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t acc = (jt > 0 || kk > 0) ? 1u : 0u;
+            if (elect_one())
+              umma_ts(tmem + C::T_DV, tmem + C::T_P + kk * 8, ddo + kk * KSTEP16, id_kv, acc);
+            if (elect_one())
+              umma_ts(tmem + C::T_DK, tmem + C::T_DS + kk * 8, dq + kk * KSTEP16, id_kv, acc);
+          }
+          if (elect_one()) {
+            umma_commit(&bar_qd_empty[qs]);
+            umma_commit(&bar_mma_done);
+          }
+          __syncwarp();
+        }
+      }
+    } else {
+      // dQ partial = dS K (K dimension = keys) once dS is in shared memory
+      // and the compute threads have read the buffer's previous partial
+      constexpr uint32_t id_q = idesc_bf16(128, D, 1, 1);  // A=dS (smem, MN-major)
+      const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
       const uint64_t dds0 = umma_desc(smem_u32(smem + C::OFF_DS), 16384, 1024, kSw128);
-      constexpr uint32_t TILE16 = C::TILE >> 4, KSTEP16 = (16 * C::ROW) >> 4;
-      // cursors: tile index, its query tile jt, its item n, Q/dO stage, phase
-      struct Cur { int t, jt, n, qs, qph; };
-      auto advance = [&](Cur& c) {
-        ++c.t;
-        if (++c.jt == njt) { c.jt = 0; ++c.n; }
-        if (++c.qs == C::NQ) { c.qs = 0; c.qph ^= 1; }
-      };
-      Cur ca{0, 0, 0, 0, 0}, cb{0, 0, 0, 0, 0};  // next S/dP tile, next dV/dK/dQ tile
-      Watchdog wd;
-      wd.reset();
-      while (cb.t < total) {
-        bool prog = false;
-        // S/dP of tile t+1 go out as soon as the compute threads hold S/dP of
-        // tile t, ahead of dV/dK/dQ of tile t: the tensor core then computes
-        // them while tile t's softmax runs (Q/dO stages: t, t+1 and t+2 live)
-        if (ca.t < total && ca.t <= cb.t + 2) {
-          const int kvs = ca.n & 1;
-          const bool ready = (ca.t == 0 || mbar_test(&bar_sdp_free, (ca.t - 1) & 1)) &&
-                             mbar_test(&bar_qd_full[ca.qs], ca.qph) &&
-                             (ca.jt != 0 || mbar_test(&bar_kv_full[kvs], (ca.n >> 1) & 1));
-          if (__any_sync(0xffffffffu, ready)) {
-            tc_fence_after();
-            const uint64_t dk = dk0 + kvs * TILE16, dv = dv0 + kvs * TILE16;
-            const uint64_t dq = dq0 + ca.qs * TILE16, ddo = ddo0 + ca.qs * TILE16;
+      int g = 0;
+      for (int n = 0; n < my_items && ok; ++n) {
+        const int kvs = n & 1;
+        for (int jt = 0; jt < njt; ++jt, ++g) {
+          ok = mbar_wait(&bar_p_ready, g & 1, wctx);
+          if (ok && g >= 2) ok = mbar_wait(&bar_dq_free[g & 1], ((g >> 1) - 1) & 1, wctx);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t dk = dk0 + kvs * TILE16;
+          const uint32_t dqt = tmem + C::T_DQ + (g & 1) * D;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              if (elect_one()) umma_ss(tmem + C::T_S, dk + 2 * kk, dq + 2 * kk, id_sdp, kk > 0);
-              if (elect_one()) umma_ss(tmem + C::T_DP, dv + 2 * kk, ddo + 2 * kk, id_sdp, kk > 0);
-            }
-            if (elect_one()) umma_commit(&bar_s_full);
-            __syncwarp();
-            advance(ca);
-            prog = true;
+          for (int kk = 0; kk < 8; ++kk)
+            if (elect_one()) umma_ss(dqt, dds0 + kk * (2048 >> 4), dk + kk * KSTEP16, id_q, kk > 0);
+          if (elect_one()) {
+            if (jt == njt - 1) umma_commit(&bar_kv_empty[kvs]);
+            umma_commit(&bar_mma_done);
           }
-        }
-        if (cb.t < ca.t) {
-          const int kvs = cb.n & 1, bq = cb.t;
-          const bool ready = mbar_test(&bar_p_ready, bq & 1) &&
-              (bq < 2 || mbar_test(&bar_dq_free[bq & 1], ((bq >> 1) - 1) & 1)) &&
-              (cb.jt != 0 || cb.n == 0 || mbar_test(&bar_dkdv_free, (cb.n - 1) & 1));
-          if (__any_sync(0xffffffffu, ready)) {
-            tc_fence_after();
-            const uint64_t dq = dq0 + cb.qs * TILE16, ddo = ddo0 + cb.qs * TILE16;
-            const uint64_t dk = dk0 + kvs * TILE16;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t acc = (cb.jt > 0 || kk > 0) ? 1u : 0u;
-              // dV += P^T dOa ; dK += dS^T Q  (K dimension = queries, 16 per step)
-              if (elect_one())
-                umma_ts(tmem + C::T_DV, tmem + C::T_P + kk * 8, ddo + kk * KSTEP16, id_kv, acc);
-              if (elect_one())
-                umma_ts(tmem + C::T_DK, tmem + C::T_DS + kk * 8, dq + kk * KSTEP16, id_kv, acc);
-            }
-            const uint32_t dqt = tmem + C::T_DQ + (bq & 1) * D;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // dQ = dS K  (K dimension = keys)
-              if (elect_one()) umma_ss(dqt, dds0 + kk * (2048 >> 4), dk + kk * KSTEP16, id_q, kk > 0);
-            if (elect_one()) {
-              umma_commit(&bar_qd_empty[cb.qs]);
-              if (cb.jt == njt - 1) umma_commit(&bar_kv_empty[kvs]);
-              umma_commit(&bar_mma_done);
-            }
-            __syncwarp();
-            advance(cb);
-            prog = true;
-          }
-        }
-        if (prog) {
-          wd.reset();
-        } else if (!__all_sync(0xffffffffu, wd.poll(wctx))) {
-          break;
+          __syncwarp();
         }
       }
-      if (elect_one()) umma_commit(&bar_drain);
-      __syncwarp();
-      if (lane == 0) {
-        volatile int no_abort = 0;
-        mbar_wait(&bar_drain, 0, &no_abort);
-      }
+    }
+    // every issued MMA completes before TMEM can be released
+    if (elect_one()) umma_commit(&bar_drain[warp - 1]);
+    __syncwarp();
+    if (lane == 0) {
+      volatile int no_abort = 0;
+      mbar_wait(&bar_drain[warp - 1], 0, &no_abort);
     }
     __syncwarp();
   }
-  // warps 2-3 have no role
   teardown();
   } else {
     // ============================ compute ==================================
