@@ -28,8 +28,9 @@
 // Warp roles (384 threads, three warpgroups):
 //   warp 0      TMA producer: Q tiles, K/V tiles of each (kt, s) and the
 //               additive key mask of that (s, kt)
-//   warps 1-2   MMA issuers of softmax warpgroups 0 and 1: T per tile, then
-//               O += P V with P read from tensor memory
+//   warp 1      MMA issuer of T, every tile in order
+//   warp 2      MMA issuer of O += P V (P read from tensor memory), every
+//               tile in order
 //   warp 3      TMA producer of the bias tile of each kt
 //   warps 4-7   softmax warpgroup 0: rows s = 0, 2, ... of the group
 //   warps 8-11  softmax warpgroup 1: rows s = 1, 3, ...
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < C::NS; ++i) { mbar_init(&bar_kv_full[i], 1); mbar_init(&bar_kv_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_bias_full[i], 1);
-      mbar_init(&bar_bias_empty[i], n_wg);  // each active issuer, after its last tile of a kt
+      mbar_init(&bar_bias_empty[i], 1);  // after the last T of a kt
       mbar_init(&bar_s_full[i], 1);
       mbar_init(&bar_p_ready[i], 128);
       mbar_init(&bar_drain[i], 1);
@@ -295,112 +296,93 @@ __global__ void __launch_bounds__(384, 1)
     }
     __syncwarp();
   } else if (warp <= 2) {
-    // =================== MMA issuers (warp 1: warpgroup 0, warp 2: 1) ======
-    // Each waits (suspended in mbarrier.try_wait) for exactly the event its
-    // next MMA needs.  Order per warpgroup: T of its next tile goes out
-    // before O += P V of its current one, so the T buffer pool lets the
-    // tensor core compute a warpgroup's next logits while it still works on
-    // the current ones.  The whole warp runs the loop (descriptors stay
-    // warp-uniform); the elected lane, the same one throughout (the warp stays
-    // converged), issues each tcgen05.mma and commit.
-    const int w = warp - 1;
-    constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q, K both K-major
-    constexpr uint32_t id_b = idesc_bf16(128, 128, 0, BIAS_K_CONTIG ? 1 : 0);
-    constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);    // P from TMEM, V MN-major
-    const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
+    // =================== MMA issuers ======================================
+    // Warp 1 issues T of every tile, warp 2 O += P V of every tile, both in
+    // tile order i = kt*g_eff + s (row s belongs to softmax warpgroup s & 1).
+    // Each waits (suspended in mbarrier.try_wait) for exactly the events its
+    // next MMAs need, so a T waits only for its K/V stage, its bias tile and
+    // the PV that frees its buffer, and a PV only for its P.  The whole warp
+    // runs the loop (descriptors stay warp-uniform); the elected lane, the
+    // same one throughout (the warp stays converged), issues each
+    // tcgen05.mma and commit.
     const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
     const uint64_t dv0 = umma_desc(smem_u32(smem + C::OFF_V), 16, C::ATOM, C::SW);
-    const uint64_t dz0 = umma_desc(smem_u32(smem + C::OFF_Z), 16, 256, kSw32);
-    // bias tile as the B operand (N = keys, K = queries j'): keys contiguous
-    // -> MN-major, 64-key halves 16 KB apart, 8 j'-rows per 1 KB; queries
-    // contiguous -> K-major rows of 64 j' per 128 B, halves 16 KB apart
-    const uint64_t dbias0 = BIAS_K_CONTIG
-                                ? umma_desc(smem_u32(smem + C::OFF_BIAS), 16384, 1024, kSw128)
-                                : umma_desc(smem_u32(smem + C::OFF_BIAS), 16, 1024, kSw128);
     bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_q, 0, wctx));
-    const int s_last = w < g_eff ? w + 2 * ((g_eff - 1 - w) / 2) : -1;  // last own row of a kt
-    // cursor over this warpgroup's tiles (kt, s), s = w, w+2, ...
-    struct Cur { int kt, s, i; };
-    auto next = [&](Cur c) {
-      c.s += 2;
-      if (c.s >= g_eff) { c.s = w; ++c.kt; }
-      c.i = c.kt * g_eff + c.s;
-      return c;
-    };
-    auto issue_t = [&](const Cur& c) {
-      const int st = c.i % C::NS, buf = c.i % C::NT;
-      bool r = mbar_wait(&bar_kv_full[st], (c.i / C::NS) & 1, wctx);
-      if (r && c.i >= C::NT) r = mbar_wait(&bar_s_free[buf], ((c.i / C::NT) - 1) & 1, wctx);
-      if (r) r = mbar_wait(&bar_bias_full[c.kt & 1], (c.kt >> 1) & 1, wctx);
-      if (!__all_sync(0xffffffffu, r)) return false;
-      tc_fence_after();
-      const uint32_t tb = tmem + 128 * buf;
-      const uint64_t dq = dq0 + ((uint32_t)(c.s * C::TILE) >> 4);
-      const uint64_t dk = dk0 + ((uint32_t)(st * C::TILE) >> 4);
+    if (warp == 1) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, 0, 0);  // Q, K both K-major
+      constexpr uint32_t id_b = idesc_bf16(128, 128, 0, BIAS_K_CONTIG ? 1 : 0);
+      const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
+      const uint64_t dz0 = umma_desc(smem_u32(smem + C::OFF_Z), 16, 256, kSw32);
+      // bias tile as the B operand (N = keys, K = queries j'): keys contiguous
+      // -> MN-major, 64-key halves 16 KB apart, 8 j'-rows per 1 KB; queries
+      // contiguous -> K-major rows of 64 j' per 128 B, halves 16 KB apart
+      const uint64_t dbias0 = BIAS_K_CONTIG
+                                  ? umma_desc(smem_u32(smem + C::OFF_BIAS), 16384, 1024, kSw128)
+                                  : umma_desc(smem_u32(smem + C::OFF_BIAS), 16, 1024, kSw128);
+      for (int kt = 0, i = 0; kt < nkt && ok; ++kt) {
+        for (int s = 0; s < g_eff; ++s, ++i) {
+          const int st = i % C::NS, buf = i % C::NT;
+          ok = mbar_wait(&bar_kv_full[st], (i / C::NS) & 1, wctx);
+          if (ok && i >= C::NT) ok = mbar_wait(&bar_s_free[buf], ((i / C::NT) - 1) & 1, wctx);
+          if (ok && s == 0) ok = mbar_wait(&bar_bias_full[kt & 1], (kt >> 1) & 1, wctx);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tb = tmem + 128 * buf;
+          const uint64_t dq = dq0 + ((uint32_t)(s * C::TILE) >> 4);
+          const uint64_t dk = dk0 + ((uint32_t)(st * C::TILE) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        if (elect_one()) umma_ss(tb, dq + 2 * kk, dk + 2 * kk, id_s, kk > 0);
-      const uint64_t db = dbias0 + ((uint32_t)((c.kt & 1) * C::BIAS_TILE) >> 4);
+          for (int kk = 0; kk < D / 16; ++kk)
+            if (elect_one()) umma_ss(tb, dq + 2 * kk, dk + 2 * kk, id_s, kk > 0);
+          const uint64_t db = dbias0 + ((uint32_t)((kt & 1) * C::BIAS_TILE) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t a = dz0 + ((uint32_t)((112 - 16 * kk) * 32) >> 4);
-        const uint64_t bb = BIAS_K_CONTIG
-                                ? db + ((uint32_t)(kk * 2048) >> 4)
-                                : db + ((uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-        if (elect_one()) umma_ss(tb, a, bb, id_b, 1u);
-      }
-      if (elect_one()) {
-        umma_commit(&bar_s_full[w]);
-        if (c.s == s_last) umma_commit(&bar_bias_empty[c.kt & 1]);
-      }
-      __syncwarp();
-      return true;
-    };
-    auto issue_pv = [&](const Cur& c, int n) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar_p_ready[w], n & 1, wctx))) return false;
-      tc_fence_after();
-      const int st = c.i % C::NS, buf = c.i % C::NT;
-      const uint64_t dv = dv0 + ((uint32_t)(st * C::TILE) >> 4);
-      const uint32_t o = tmem + C::TMEM_O + c.s * D, pa = tmem + 128 * buf;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        if (elect_one())
-          umma_ts(o, pa + kk * 8, dv + kk * (16 * C::ROW >> 4), id_o,
-                  (c.kt > 0 || kk > 0) ? 1u : 0u);
-      if (elect_one()) {
-        umma_commit(&bar_kv_empty[st]);
-        umma_commit(&bar_o_done[c.s]);
-        umma_commit(&bar_s_free[buf]);
-      }
-      __syncwarp();
-      return true;
-    };
-    if (w < g_eff) {
-      const int my_total = nkt * ((g_eff - w + 1) / 2);
-      Cur cur{0, w, w};
-      if (ok) ok = issue_t(cur);
-      for (int n = 0; n < my_total && ok; ++n) {
-        const Cur nx = next(cur);
-        if (n + 1 < my_total) {
-          // T of the next tile first, unless its buffer is the one whose P
-          // the current tile's PV still has to read
-          if (nx.i - C::NT == cur.i) {
-            ok = issue_pv(cur, n) && issue_t(nx);
-          } else {
-            ok = issue_t(nx) && issue_pv(cur, n);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t a = dz0 + ((uint32_t)((112 - 16 * kk) * 32) >> 4);
+            const uint64_t bb = BIAS_K_CONTIG
+                                    ? db + ((uint32_t)(kk * 2048) >> 4)
+                                    : db + ((uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+            if (elect_one()) umma_ss(tb, a, bb, id_b, 1u);
           }
-        } else {
-          ok = issue_pv(cur, n);
+          if (elect_one()) {
+            umma_commit(&bar_s_full[s & 1]);
+            if (s == g_eff - 1) umma_commit(&bar_bias_empty[kt & 1]);
+          }
+          __syncwarp();
         }
-        cur = nx;
+      }
+    } else {
+      constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);  // P from TMEM, V MN-major
+      int np0 = 0, np1 = 0;  // tiles of each warpgroup handled so far
+      for (int kt = 0, i = 0; kt < nkt && ok; ++kt) {
+        for (int s = 0; s < g_eff; ++s, ++i) {
+          const int w = s & 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_p_ready[w], (w ? np1 : np0) & 1, wctx));
+          if (!ok) break;
+          if (w) ++np1; else ++np0;
+          tc_fence_after();
+          const int st = i % C::NS, buf = i % C::NT;
+          const uint64_t dv = dv0 + ((uint32_t)(st * C::TILE) >> 4);
+          const uint32_t o = tmem + C::TMEM_O + s * D, pa = tmem + 128 * buf;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            if (elect_one())
+              umma_ts(o, pa + kk * 8, dv + kk * (16 * C::ROW >> 4), id_o,
+                      (kt > 0 || kk > 0) ? 1u : 0u);
+          if (elect_one()) {
+            umma_commit(&bar_kv_empty[st]);
+            umma_commit(&bar_o_done[s]);
+            umma_commit(&bar_s_free[buf]);
+          }
+          __syncwarp();
+        }
       }
     }
     // every issued MMA completes before TMEM can be released
-    if (elect_one()) umma_commit(&bar_drain[w]);
+    if (elect_one()) umma_commit(&bar_drain[warp - 1]);
     __syncwarp();
     if (lane == 0) {
       volatile int no_abort = 0;
-      mbar_wait(&bar_drain[w], 0, &no_abort);
+      mbar_wait(&bar_drain[warp - 1], 0, &no_abort);
     }
     __syncwarp();
   }
