@@ -576,6 +576,15 @@ __global__ void __launch_bounds__(384, 1)
                      __uint_as_float(q16[e + 2]), __uint_as_float(q16[e + 3]));
       }
     };
+    // mask byte of this thread's key in item n, loaded one item ahead so its
+    // latency never sits at an item boundary
+    auto mask_of = [&](int n) -> int {
+      if (n >= my_items || !p.mask) return 1;
+      const DkdvItem mi = item(n);
+      const int mk = mi.kt * 128 + kl;
+      return mk < p.N ? (int)p.mask[mi.b * p.msb + (int64_t)mi.s * p.mss + (int64_t)mk * p.msk] : 1;
+    };
+    int mask_next = mask_of(0);
     bool ok = true;
     int g = 0;
     for (int n = 0; n < my_items && ok; ++n) {
@@ -584,8 +593,8 @@ __global__ void __launch_bounds__(384, 1)
       // additive mask of this key, log2 units (constant over the query tiles)
       float madd = 0.f;
       if (kg >= p.N) madd = -INFINITY;
-      else if (p.mask && !p.mask[it.b * p.msb + (int64_t)it.s * p.mss + (int64_t)kg * p.msk])
-        madd = kMaskBias * kLog2e;
+      else if (!mask_next) madd = kMaskBias * kLog2e;
+      mask_next = mask_of(n + 1);
       const float2 mm = make_float2(madd, madd);
       for (int jt = 0; jt < njt; ++jt, ++g) {
         const int qs = g % C::NQ, bs = g % C::NB;

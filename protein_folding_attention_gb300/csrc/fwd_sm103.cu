@@ -492,6 +492,19 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
     // ---- epilogue: O / l, sigmoid gate, lse -------------------------------
+    // the gate rows of every row s of this warpgroup are requested before
+    // the first wait, so their latency overlaps the last PV products
+    uint4 gq[C::G / 2][D / 8];
+    if (HAS_GATE && ok && j < p.N) {
+#pragma unroll
+      for (int u = 0; u < C::G / 2; ++u) {
+        const int s = 2 * u + wg;
+        if (s >= g_eff) break;
+        const __nv_bfloat16* gsrc = p.gate + p.g.at(b, s0 + s, h, j, 0);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) gq[u][c] = *reinterpret_cast<const uint4*>(gsrc + 8 * c);
+      }
+    }
     if (ok) {
 #pragma unroll
       for (int u = 0; u < C::G / 2; ++u) {
@@ -515,16 +528,15 @@ __global__ void __launch_bounds__(384, 1)
           const int64_t row_id = (((int64_t)b * p.S + ss) * p.H + h) * p.N + j;
           p.lse[row_id] = (m_run[u] * c1 + __log2f(l_run[u])) * kLn2;
           __nv_bfloat16* dst = p.out + p.o.at(b, ss, h, j, 0);
-          const __nv_bfloat16* gsrc = HAS_GATE ? p.gate + p.g.at(b, ss, h, j, 0) : nullptr;
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) {
             float gv[8];
             if (HAS_GATE) {
-              const uint4 g4 = *reinterpret_cast<const uint4*>(gsrc + 8 * c);
+              const uint4 g4 = gq[u][c];
               gv[0] = bf16lo(g4.x); gv[1] = bf16hi(g4.x); gv[2] = bf16lo(g4.y); gv[3] = bf16hi(g4.y);
               gv[4] = bf16lo(g4.z); gv[5] = bf16hi(g4.z); gv[6] = bf16lo(g4.w); gv[7] = bf16hi(g4.w);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) gv[e] = inv_l / (1.0f + ex2(-gv[e] * kLog2e));
+              for (int e = 0; e < 8; ++e) gv[e] = __fdividef(inv_l, 1.0f + ex2(-gv[e] * kLog2e));
             } else {
 #pragma unroll
               for (int e = 0; e < 8; ++e) gv[e] = inv_l;
