@@ -162,16 +162,23 @@ struct Tile {
   static constexpr uint32_t BIAS_TILE = 128 * 128 * 2;
 };
 
-// bias[j, k] of a 128x128 tile staged by TMA as two 64-wide boxes with a
-// 128-byte swizzle.  K_CONTIG: rows are j (keys contiguous), otherwise rows
-// are k (queries contiguous).
-template <bool K_CONTIG>
-__device__ __forceinline__ float bias_at(const uint8_t* tile, int j, int k) {
-  const int r = K_CONTIG ? j : k;   // smem row
-  const int c = K_CONTIG ? k : j;   // contiguous index
-  const uint8_t* p = tile + (c >> 6) * 16384 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) +
-                     (c & 7) * 2;
-  return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(p)) << 16);
+// The pair bias enters the logit tiles through the tensor core, as in the
+// forward: T = Q K^T + (c I) * bias with c = sqrt(D) rounded to bf16, the
+// identity never stored whole but as 128-row windows (start row 112 - 16 kk
+// for reduction chunk kk) of a 240 x 16 matrix Z with Z[112 + i][i] = c,
+// kept in the 32-byte-swizzled K-major layout.  The backward so recomputes
+// exactly the logits whose logsumexp the forward stored.
+constexpr uint32_t kZBytes = 240 * 32;
+__device__ __forceinline__ void write_identity_windows(uint8_t* z, int D, int tid, int nthreads) {
+  const uint32_t cb = __bfloat16_as_ushort(__float2bfloat16_rn(sqrtf((float)D)));
+  uint32_t* z32 = reinterpret_cast<uint32_t*>(z);
+  for (int i = tid; i < (int)(kZBytes / 4); i += nthreads) {
+    const int r = i >> 3, wd = i & 7;
+    const int c0 = (((wd >> 2) ^ ((r >> 2) & 1)) << 3) + ((wd & 3) << 1);
+    const int one = r - 112;  // column of this row's nonzero, if any
+    z32[i] = one == c0 ? cb : (one == c0 + 1 ? cb << 16 : 0u);
+  }
+  fence_proxy_async_smem();  // generic writes, read by the tensor core
 }
 
 // ---------------------------------------------------------------------------
@@ -194,23 +201,22 @@ template <int D, bool BIAS_K_CONTIG>
 struct DkdvCfg : Tile<D> {
   using T = Tile<D>;
   static constexpr int NQ = 3;  // Q/dO/(lse,delta) stages
-  // bias stages: a key-row-major bias needs no staging buffer, which leaves
-  // room for a third stage
-  static constexpr int NB = BIAS_K_CONTIG ? 2 : 3;
+  static constexpr int NB = 3;  // bias stages (as the TMA delivers them)
   static constexpr uint32_t OFF_K = 0;                              // 2 stages
   static constexpr uint32_t OFF_V = OFF_K + 2 * T::TILE;            // 2 stages
   static constexpr uint32_t OFF_Q = OFF_V + 2 * T::TILE;
   static constexpr uint32_t OFF_DO = OFF_Q + NQ * T::TILE;
-  static constexpr uint32_t OFF_BIAS = OFF_DO + NQ * T::TILE;      // rows = key k
-  static constexpr uint32_t OFF_RAW = OFF_BIAS + NB * T::BIAS_TILE;
-  static constexpr uint32_t OFF_DS = OFF_RAW + (BIAS_K_CONTIG ? T::BIAS_TILE : 0);
-  static constexpr uint32_t OFF_LD = OFF_DS + 128 * 128 * 2;  // -lse2[128], -delta/sqrt(D)[128]
+  static constexpr uint32_t OFF_BIAS = OFF_DO + NQ * T::TILE;
+  static constexpr uint32_t OFF_DS = OFF_BIAS + NB * T::BIAS_TILE;
+  static constexpr uint32_t OFF_Z = OFF_DS + 128 * 128 * 2;
+  static constexpr uint32_t OFF_LD = OFF_Z + kZBytes;  // -lse2[128], -delta/sqrt(D)[128]
   static constexpr uint32_t SMEM = OFF_LD + NQ * 256 * 4;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_P = 256, T_DS = 320, T_DQ = 384,
                             T_DK = 384 + 2 * D, T_DV = 384 + 3 * D;
   static_assert(T_DV + D <= 512, "tensor memory overflow");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory overflow");
+  static_assert(OFF_BIAS % 1024 == 0 && OFF_DS % 1024 == 0 && OFF_Z % 256 == 0, "alignment");
   static constexpr int THREADS = 384;
   static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 224;
   static_assert(REGS_LOW * 128 + REGS_HIGH * 256 <= LAUNCH_REGS * THREADS, "register split");
@@ -243,7 +249,7 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_kv_full[2], bar_kv_empty[2], bar_qd_full[C::NQ], bar_qd_empty[C::NQ],
-      bar_b_full[C::NB], bar_b_empty[C::NB], bar_raw, bar_s_full, bar_sdp_free, bar_p_ready,
+      bar_b_full[C::NB], bar_b_empty[C::NB], bar_s_full, bar_sdp_free, bar_p_ready,
       bar_mma_done, bar_dq_free[2], bar_dkdv_free, bar_drain[3];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -272,14 +278,15 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bar_dq_free[i], 256);
     }
     for (int i = 0; i < C::NQ; ++i) { mbar_init(&bar_qd_full[i], 1); mbar_init(&bar_qd_empty[i], 1); }
-    for (int i = 0; i < C::NB; ++i) { mbar_init(&bar_b_full[i], 1); mbar_init(&bar_b_empty[i], 256); }
-    mbar_init(&bar_raw, 1);
+    // a bias stage is free once the MMAs of its tile have read it
+    for (int i = 0; i < C::NB; ++i) { mbar_init(&bar_b_full[i], 1); mbar_init(&bar_b_empty[i], 1); }
     mbar_init(&bar_s_full, 1); mbar_init(&bar_sdp_free, 256); mbar_init(&bar_p_ready, 256);
     // dV/dK and dQ of a tile are committed by two issuers
     mbar_init(&bar_mma_done, 2); mbar_init(&bar_dkdv_free, 256);
     for (int i = 0; i < 3; ++i) mbar_init(&bar_drain[i], 1);
     fence_barrier_init();
   }
+  write_identity_windows(smem + C::OFF_Z, D, threadIdx.x, C::THREADS);
   if (warp == 1) tmem_alloc(&tmem_slot, 512);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
@@ -306,10 +313,8 @@ __global__ void __launch_bounds__(384, 1)
   regs_dec<C::REGS_LOW>();
   if (warp == 0) {
     // ============================ producer =================================
-    // The compute threads read the bias tile by key rows.  A key-row-major
-    // tile (queries contiguous: the ending-node view) is fetched straight
-    // into its stage; a query-row-major one is staged and transposed.
-    // Copies issued by one thread are served in order, those of different
+    // The bias tile goes to its stage as the TMA delivers it (the MMA reads
+    // either layout).  Copies issued by one thread are served in order, those of different
     // threads concurrently: each box is issued by the next lane in turn (the
     // whole warp calls issue_bias; lane 0 arms the barrier first).
     int rr = 0;
@@ -330,11 +335,7 @@ __global__ void __launch_bounds__(384, 1)
     };
     const float inv_sqrt_d = rsqrtf((float)D);
     bool ok = true;
-    int kv_issued = 0, qd_issued = 0, b_issued = 0, raw_issued = 0;
-    if (BIAS_K_CONTIG && total > 0) {
-      issue_bias(0, smem + C::OFF_RAW, &bar_raw);
-      raw_issued = 1;
-    }
+    int kv_issued = 0, qd_issued = 0, b_issued = 0;
     // The per-query constants of tile g+1 are loaded into registers while
     // tile g is being armed, so the producer never waits on their latency.
     float pre_l[4], pre_d[4];
@@ -399,20 +400,8 @@ __global__ void __launch_bounds__(384, 1)
         if (g >= C::NB) ok = mbar_wait(&bar_b_empty[bs], ((g / C::NB) - 1) & 1, wctx);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        uint8_t* stage = smem + C::OFF_BIAS + bs * C::BIAS_TILE;
-        if (!BIAS_K_CONTIG) {
-          issue_bias(g, stage, &bar_b_full[bs]);
-          b_issued = g + 1;
-        } else {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw, g & 1, wctx));
-          if (!ok) break;
-          transpose_tile128_bf16(smem + C::OFF_RAW, stage, lane);
-          fence_proxy_async_smem();  // generic reads of the staging buffer before its next TMA
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_b_full[bs]);
-          if (g + 1 < total) issue_bias(g + 1, smem + C::OFF_RAW, &bar_raw);
-          if (g + 1 < total) raw_issued = g + 2;
-        }
+        issue_bias(g, smem + C::OFF_BIAS + bs * C::BIAS_TILE, &bar_b_full[bs]);
+        b_issued = g + 1;
       }
     }
     // After a give-up, let every copy already issued land before the CTA may
@@ -426,7 +415,6 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait(&bar_qd_full[i % C::NQ], (i / C::NQ) & 1, &no_abort);
       for (int i = max(0, b_issued - C::NB); i < b_issued; ++i)
         mbar_wait(&bar_b_full[i % C::NB], (i / C::NB) & 1, &no_abort);
-      if (raw_issued > 0) mbar_wait(&bar_raw, (raw_issued - 1) & 1, &no_abort);
     }
     __syncwarp();
   } else {
@@ -440,22 +428,32 @@ __global__ void __launch_bounds__(384, 1)
     constexpr uint32_t TILE16 = C::TILE >> 4, KSTEP16 = (16 * C::ROW) >> 4;
     bool ok = true;
     if (warp == 1) {
-      // S^T = K Q^T and dP^T = V dOa^T once Q/dOa (and, on an item's first
-      // tile, K/V) are loaded and S/dP of the previous tile are in the
-      // compute threads' registers
+      // S^T = K Q^T + (c I) bias^T and dP^T = V dOa^T once Q/dOa, the bias
+      // tile (and, on an item's first tile, K/V) are loaded and S/dP of the
+      // previous tile are in the compute threads' registers
       constexpr uint32_t id_sdp = idesc_bf16(128, 128, 0, 0);  // A=K/V, B=Q/dOa, K-major
+      // bias tile as the B operand (N = queries j, K = keys k'): keys
+      // contiguous -> K-major rows of 64 k' per 128 B, halves 16 KB apart;
+      // queries contiguous -> MN-major, 64-query halves 16 KB apart, 8
+      // k'-rows per 1 KB
+      constexpr uint32_t id_b = idesc_bf16(128, 128, 0, BIAS_K_CONTIG ? 0 : 1);
       const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
       const uint64_t dv0 = umma_desc(smem_u32(smem + C::OFF_V), 16, C::ATOM, C::SW);
       const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
       const uint64_t ddo0 = umma_desc(smem_u32(smem + C::OFF_DO), 16, C::ATOM, C::SW);
+      const uint64_t dz0 = umma_desc(smem_u32(smem + C::OFF_Z), 16, 256, kSw32);
+      const uint64_t dbias0 = BIAS_K_CONTIG
+                                  ? umma_desc(smem_u32(smem + C::OFF_BIAS), 16, 1024, kSw128)
+                                  : umma_desc(smem_u32(smem + C::OFF_BIAS), 16384, 1024, kSw128);
       int g = 0;
       for (int n = 0; n < my_items && ok; ++n) {
         const int kvs = n & 1;
         for (int jt = 0; jt < njt; ++jt, ++g) {
-          const int qs = g % C::NQ;
+          const int qs = g % C::NQ, bs = g % C::NB;
           ok = mbar_wait(&bar_qd_full[qs], (g / C::NQ) & 1, wctx);
           if (ok && jt == 0) ok = mbar_wait(&bar_kv_full[kvs], (n >> 1) & 1, wctx);
           if (ok && g > 0) ok = mbar_wait(&bar_sdp_free, (g - 1) & 1, wctx);
+          if (ok) ok = mbar_wait(&bar_b_full[bs], (g / C::NB) & 1, wctx);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
@@ -466,7 +464,19 @@ __global__ void __launch_bounds__(384, 1)
             if (elect_one()) umma_ss(tmem + C::T_S, dk + 2 * kk, dq + 2 * kk, id_sdp, kk > 0);
             if (elect_one()) umma_ss(tmem + C::T_DP, dv + 2 * kk, ddo + 2 * kk, id_sdp, kk > 0);
           }
-          if (elect_one()) umma_commit(&bar_s_full);
+          const uint64_t db = dbias0 + ((uint32_t)(bs * C::BIAS_TILE) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t a = dz0 + ((uint32_t)((112 - 16 * kk) * 32) >> 4);
+            const uint64_t bb = BIAS_K_CONTIG
+                                    ? db + ((uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4)
+                                    : db + ((uint32_t)(kk * 2048) >> 4);
+            if (elect_one()) umma_ss(tmem + C::T_S, a, bb, id_b, 1u);
+          }
+          if (elect_one()) {
+            umma_commit(&bar_s_full);
+            umma_commit(&bar_b_empty[bs]);
+          }
           __syncwarp();
         }
       }
@@ -597,10 +607,9 @@ __global__ void __launch_bounds__(384, 1)
       mask_next = mask_of(n + 1);
       const float2 mm = make_float2(madd, madd);
       for (int jt = 0; jt < njt; ++jt, ++g) {
-        const int qs = g % C::NQ, bs = g % C::NB;
+        const int qs = g % C::NQ;
         ok = mbar_wait(&bar_s_full, g & 1, wctx) &&
-             mbar_wait(&bar_qd_full[qs], (g / C::NQ) & 1, wctx) &&
-             mbar_wait(&bar_b_full[bs], (g / C::NB) & 1, wctx);
+             mbar_wait(&bar_qd_full[qs], (g / C::NQ) & 1, wctx);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -614,13 +623,9 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_before();
         mbar_arrive(&bar_sdp_free);
         const float* ld = reinterpret_cast<const float*>(smem + C::OFF_LD + qs * 1024);
-        // bias row of this key, this warpgroup's 64 queries (one 64-wide box)
-        const uint8_t* brow = smem + C::OFF_BIAS + bs * C::BIAS_TILE + wg * 16384 + kl * 128;
         uint32_t pk[32], dk2[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {  // 8 queries per step
-          const uint4 w4 = *reinterpret_cast<const uint4*>(brow + ((c ^ (kl & 7)) << 4));
-          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
           const float4 la = *reinterpret_cast<const float4*>(ld + 64 * wg + 8 * c);
           const float4 lb = *reinterpret_cast<const float4*>(ld + 64 * wg + 8 * c + 4);
           const float4 da = *reinterpret_cast<const float4*>(ld + 128 + 64 * wg + 8 * c);
@@ -632,9 +637,9 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j2 = 8 * c + 2 * e;
+            // S already holds the pair bias (scaled by c = bf16(sqrt(D)))
             float2 t = fma2(make_float2(__uint_as_float(sx[j2]), __uint_as_float(sx[j2 + 1])),
                             c1c1, mm);
-            t = fma2(make_float2(bf16lo(wv[e]), bf16hi(wv[e])), l2l2, t);
             t = add2(t, nl[e]);
             const float2 pr = make_float2(ex2(t.x), ex2(t.y));
             const float2 gg = fma2(
@@ -644,7 +649,6 @@ __global__ void __launch_bounds__(384, 1)
             dk2[4 * c + e] = pack_bf16(ds.x, ds.y);
           }
         }
-        mbar_arrive(&bar_b_empty[bs]);
         // the previous tile's MMAs read P^T, dS^T and the dS tile: wait for them
         if (g > 0) {
           ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done, (g - 1) & 1, wctx));
@@ -707,8 +711,8 @@ __global__ void __launch_bounds__(384, 1)
 // owns query j (TMEM lane) and the 64 keys of its warpgroup's half.  Tensor
 // memory: S 0..127, dP 128..255 (fp32, lane =
 // query); each compute thread keeps its 64 dbias sums in registers across
-// the slot's s.  The bias tile is fetched once per CTA with query rows
-// (transposed in shared memory when the view has queries contiguous).
+// the slot's s.  The bias tile is fetched once per CTA as the TMA delivers
+// it and added into every S tile by the identity-window MMAs.
 template <int D>
 struct DbiasCfg : Tile<D> {
   using T = Tile<D>;
@@ -718,9 +722,10 @@ struct DbiasCfg : Tile<D> {
   static constexpr uint32_t OFF_K = OFF_DO + NST * T::TILE;
   static constexpr uint32_t OFF_V = OFF_K + NST * T::TILE;
   static constexpr uint32_t OFF_BIAS = OFF_V + NST * T::TILE;
-  static constexpr uint32_t OFF_RAW = OFF_BIAS + T::BIAS_TILE;
-  static constexpr uint32_t OFF_MADD = OFF_RAW + T::BIAS_TILE;
-  static constexpr uint32_t SMEM = OFF_MADD + NST * 128 * 4;
+  static constexpr uint32_t OFF_Z = OFF_BIAS + T::BIAS_TILE;
+  static constexpr uint32_t OFF_MADD = OFF_Z + kZBytes;
+  static constexpr uint32_t OFF_FLAG = OFF_MADD + NST * 128 * 4;  // per stage: any masked key
+  static constexpr uint32_t SMEM = OFF_FLAG + NST * 16;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory overflow");
   static constexpr uint32_t T_S = 0, T_DP = 128;
@@ -749,8 +754,8 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t bar_bias, bar_raw, bar_full[C::NST], bar_empty[C::NST], bar_s_full,
-      bar_sdp_free, bar_drain;
+  __shared__ uint64_t bar_bias, bar_full[C::NST], bar_empty[C::NST], bar_s_full, bar_sdp_free,
+      bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -769,13 +774,13 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_bias, 1);
-    mbar_init(&bar_raw, 1);
     // a stage is empty once its MMAs completed (one commit) and both compute
     // warpgroups are done with its key mask (256 arrivals)
     for (int i = 0; i < C::NST; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_empty[i], 257); }
     mbar_init(&bar_s_full, 1); mbar_init(&bar_sdp_free, 256); mbar_init(&bar_drain, 1);
     fence_barrier_init();
   }
+  write_identity_windows(smem + C::OFF_Z, D, threadIdx.x, C::THREADS);
   if (warp == 1) tmem_alloc(&tmem_slot, 512);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q); tma_prefetch_desc(&tm_k); tma_prefetch_desc(&tm_v);
@@ -806,8 +811,8 @@ __global__ void __launch_bounds__(384, 1)
     {
       // copies issued by one thread are served in order, those of different
       // threads concurrently: each box goes out from its own lane
-      uint8_t* dst = smem + (BIAS_K_CONTIG ? C::OFF_BIAS : C::OFF_RAW);
-      uint64_t* bar = BIAS_K_CONTIG ? &bar_bias : &bar_raw;
+      uint8_t* dst = smem + C::OFF_BIAS;
+      uint64_t* bar = &bar_bias;
       if (lane == 0) mbar_arrive_expect_tx(bar, C::BIAS_TILE);
       __syncwarp();
       if (BIAS_K_CONTIG) {
@@ -837,6 +842,7 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       float* madd = reinterpret_cast<float*>(smem + C::OFF_MADD + st * 512);
+      bool any = false;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int kk = kt * 128 + e * 32 + lane;
@@ -844,7 +850,10 @@ __global__ void __launch_bounds__(384, 1)
         if (kk >= p.N) a = -INFINITY;
         else if (p.mask && !pre_m[e]) a = kMaskBias * kLog2e;
         madd[e * 32 + lane] = a;
+        any |= a != 0.f;
       }
+      any = __any_sync(0xffffffffu, any);
+      if (lane == 0) *reinterpret_cast<int*>(smem + C::OFF_FLAG + st * 16) = any ? 1 : 0;
       prefetch_mask(i + 1);
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&bar_full[st], 4 * C::TILE);
@@ -861,20 +870,12 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_5d(smem + C::OFF_V + st * C::TILE, &tm_v, &bar_full[st], 0, kt * 128, h, s, b);
       }
       issued = i + 1;
-      if (!BIAS_K_CONTIG && i == 0) {
-        // query-contiguous bias: transpose the staged tile into query rows
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw, 0, wctx));
-        if (!ok) break;
-        transpose_tile128_bf16(smem + C::OFF_RAW, smem + C::OFF_BIAS, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_bias);
-      }
     }
     if (!ok && lane == 0) {
       volatile int no_abort = 0;
       for (int i = max(0, issued - C::NST); i < issued; ++i)
         mbar_wait(&bar_full[i % C::NST], (i / C::NST) & 1, &no_abort);
-      mbar_wait(BIAS_K_CONTIG ? &bar_bias : &bar_raw, 0, &no_abort);
+      mbar_wait(&bar_bias, 0, &no_abort);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -882,11 +883,17 @@ __global__ void __launch_bounds__(384, 1)
     // whole warp, elected lane issues (as in the dK/dV kernel)
     {
       constexpr uint32_t id = idesc_bf16(128, 128, 0, 0);
+      // bias tile as the B operand (N = keys, K = queries j'), as in the forward
+      constexpr uint32_t id_b = idesc_bf16(128, 128, 0, BIAS_K_CONTIG ? 1 : 0);
       const uint64_t dq0 = umma_desc(smem_u32(smem + C::OFF_Q), 16, C::ATOM, C::SW);
       const uint64_t ddo0 = umma_desc(smem_u32(smem + C::OFF_DO), 16, C::ATOM, C::SW);
       const uint64_t dk0 = umma_desc(smem_u32(smem + C::OFF_K), 16, C::ATOM, C::SW);
       const uint64_t dv0 = umma_desc(smem_u32(smem + C::OFF_V), 16, C::ATOM, C::SW);
-      bool ok = true;
+      const uint64_t dz0 = umma_desc(smem_u32(smem + C::OFF_Z), 16, 256, kSw32);
+      const uint64_t db = BIAS_K_CONTIG
+                              ? umma_desc(smem_u32(smem + C::OFF_BIAS), 16384, 1024, kSw128)
+                              : umma_desc(smem_u32(smem + C::OFF_BIAS), 16, 1024, kSw128);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_bias, 0, wctx));
       for (int i = 0; i < ns && ok; ++i) {
         const int st = i % C::NST;
         ok = mbar_wait(&bar_full[st], (i / C::NST) & 1, wctx);
@@ -899,6 +906,14 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           if (elect_one()) umma_ss(tmem + C::T_S, dq0 + off + 2 * kk, dk0 + off + 2 * kk, id, kk > 0);
           if (elect_one()) umma_ss(tmem + C::T_DP, ddo0 + off + 2 * kk, dv0 + off + 2 * kk, id, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = dz0 + ((uint32_t)((112 - 16 * kk) * 32) >> 4);
+          const uint64_t bb = BIAS_K_CONTIG
+                                  ? db + ((uint32_t)(kk * 2048) >> 4)
+                                  : db + ((uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          if (elect_one()) umma_ss(tmem + C::T_S, a, bb, id_b, 1u);
         }
         if (elect_one()) {
           umma_commit(&bar_empty[st]);
@@ -926,10 +941,8 @@ __global__ void __launch_bounds__(384, 1)
     const int jg = jt * 128 + jl;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const float c1 = kLog2e * rsqrtf((float)D);
-    const float2 c1c1 = make_float2(c1, c1), l2l2 = make_float2(kLog2e, kLog2e);
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_bias, 0, wctx));
-    // this query's 64 bias values (one 64-wide box), query-row layout
-    const uint8_t* brow = smem + C::OFF_BIAS + wg * 16384 + jl * 128;
+    const float2 c1c1 = make_float2(c1, c1);
+    bool ok = true;
     // dbias accumulators of this thread's 64 keys, in registers across all s
     float2 acc[32];
 #pragma unroll
@@ -953,6 +966,8 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const float2 nl = make_float2(nlse2, nlse2), nd = make_float2(ndl, ndl);
       const float* madd = reinterpret_cast<const float*>(smem + C::OFF_MADD + st * 512);
+      // warp-uniform: most key tiles have no masked key
+      const bool masked = *reinterpret_cast<const int*>(smem + C::OFF_FLAG + st * 16) != 0;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t sx[32], dpx[32];
@@ -965,20 +980,22 @@ __global__ void __launch_bounds__(384, 1)
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int cc = 4 * half + c;  // 16-byte chunk: keys 64*wg + 8*cc ..
-          const uint4 w4 = *reinterpret_cast<const uint4*>(brow + ((cc ^ (jl & 7)) << 4));
-          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-          const float4 ma = *reinterpret_cast<const float4*>(madd + 64 * wg + 8 * cc);
-          const float4 mb = *reinterpret_cast<const float4*>(madd + 64 * wg + 8 * cc + 4);
-          const float2 mv[4] = {make_float2(ma.x, ma.y), make_float2(ma.z, ma.w),
-                                make_float2(mb.x, mb.y), make_float2(mb.z, mb.w)};
+          const int cc = 4 * half + c;  // keys 64*wg + 8*cc ..
+          float2 mv[4];
+          if (masked) {
+            const float4 ma = *reinterpret_cast<const float4*>(madd + 64 * wg + 8 * cc);
+            const float4 mb = *reinterpret_cast<const float4*>(madd + 64 * wg + 8 * cc + 4);
+            mv[0] = add2(make_float2(ma.x, ma.y), nl); mv[1] = add2(make_float2(ma.z, ma.w), nl);
+            mv[2] = add2(make_float2(mb.x, mb.y), nl); mv[3] = add2(make_float2(mb.z, mb.w), nl);
+          } else {
+            mv[0] = nl; mv[1] = nl; mv[2] = nl; mv[3] = nl;
+          }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int k2 = 8 * c + 2 * e;
-            float2 t = fma2(make_float2(__uint_as_float(sx[k2]), __uint_as_float(sx[k2 + 1])),
-                            c1c1, mv[e]);
-            t = fma2(make_float2(bf16lo(wv[e]), bf16hi(wv[e])), l2l2, t);
-            t = add2(t, nl);
+            // S already holds the pair bias (scaled by c = bf16(sqrt(D)))
+            const float2 t =
+                fma2(make_float2(__uint_as_float(sx[k2]), __uint_as_float(sx[k2 + 1])), c1c1, mv[e]);
             const float2 pr = make_float2(ex2(t.x), ex2(t.y));
             const float2 gg =
                 add2(make_float2(__uint_as_float(dpx[k2]), __uint_as_float(dpx[k2 + 1])), nd);

@@ -365,41 +365,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 namespace evo {
 
 // ---------------------------------------------------------------------------
-// 128x128 bf16 tile transpose in shared memory (one warp).
-// ---------------------------------------------------------------------------
-// Both tiles use the layout the TMA writes for a 128-row x 128-column bf16
-// tile fetched as two 64-column boxes with a 128-byte swizzle: element
-// (r, c) lives at  (c / 64) * 16384 + r * 128 + (((c % 64) / 8) ^ (r % 8)) * 16
-// + (c % 8) * 2.  dst(c, r) = src(r, c).  Each 8x8 block is read with
-// ldmatrix.trans (rows r of the source) and written with stmatrix (rows c of
-// the destination); 64 x4 instructions of each move the whole tile.
-__device__ __forceinline__ uint32_t swz128_chunk(uint32_t base, int r, int c8) {
-  // address of the 16-byte chunk holding columns 8*c8 .. 8*c8+7 of row r
-  return base + (uint32_t)((c8 >> 3) * 16384 + r * 128 + (((c8 & 7) ^ (r & 7)) << 4));
-}
-
-// Blocks [blk_begin, blk_begin + nblk) of the 256 8x8 blocks (nblk a
-// multiple of 4; several warps can split a tile).
-__device__ __forceinline__ void transpose_tile128_bf16(const void* src, void* dst, int lane,
-                                                       int blk_begin = 0, int nblk = 256) {
-  const uint32_t s = smem_u32(src), d = smem_u32(dst);
-  const int m = lane >> 3, i = lane & 7;  // matrix of this lane's address, row within it
-#pragma unroll 4
-  for (int it = 0; it < nblk / 4; ++it) {
-    const int blk = blk_begin + it * 4 + m;
-    const int rb = blk >> 4, cb = blk & 15;
-    uint32_t r0, r1, r2, r3;
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(swz128_chunk(s, rb * 8 + i, cb)));
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
-                     swz128_chunk(d, cb * 8 + i, rb)),
-                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-                 : "memory");
-  }
-}
-
-// ---------------------------------------------------------------------------
 // per-warpgroup register budget (all 128 threads of the warpgroup execute it)
 // ---------------------------------------------------------------------------
 template <uint32_t N>
