@@ -728,7 +728,9 @@ struct DbiasCfg : Tile<D> {
   static constexpr uint32_t SMEM = OFF_FLAG + NST * 16;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory overflow");
-  static constexpr uint32_t T_S = 0, T_DP = 128;
+  // S and dP double-buffered: buffer b at 256 b, so the MMAs of the next s
+  // run while the compute threads work on the current one
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_BUF = 256;
   static constexpr int THREADS = 384;
   static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 224;
   static_assert(REGS_LOW * 128 + REGS_HIGH * 256 <= LAUNCH_REGS * THREADS, "register split");
@@ -754,8 +756,8 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t bar_bias, bar_full[C::NST], bar_empty[C::NST], bar_s_full, bar_sdp_free,
-      bar_drain;
+  __shared__ uint64_t bar_bias, bar_full[C::NST], bar_empty[C::NST], bar_s_full[2],
+      bar_sdp_free[2], bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -777,7 +779,8 @@ __global__ void __launch_bounds__(384, 1)
     // a stage is empty once its MMAs completed (one commit) and both compute
     // warpgroups are done with its key mask (256 arrivals)
     for (int i = 0; i < C::NST; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_empty[i], 257); }
-    mbar_init(&bar_s_full, 1); mbar_init(&bar_sdp_free, 256); mbar_init(&bar_drain, 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(&bar_s_full[i], 1); mbar_init(&bar_sdp_free[i], 256); }
+    mbar_init(&bar_drain, 1);
     fence_barrier_init();
   }
   write_identity_windows(smem + C::OFF_Z, D, threadIdx.x, C::THREADS);
@@ -897,15 +900,16 @@ __global__ void __launch_bounds__(384, 1)
       for (int i = 0; i < ns && ok; ++i) {
         const int st = i % C::NST;
         ok = mbar_wait(&bar_full[st], (i / C::NST) & 1, wctx);
-        if (ok && i > 0) ok = mbar_wait(&bar_sdp_free, (i - 1) & 1, wctx);
+        if (ok && i >= 2) ok = mbar_wait(&bar_sdp_free[i & 1], ((i >> 1) - 1) & 1, wctx);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
         const uint32_t off = (uint32_t)(st * C::TILE) >> 4;
+        const uint32_t tsb = tmem + C::T_BUF * (i & 1);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          if (elect_one()) umma_ss(tmem + C::T_S, dq0 + off + 2 * kk, dk0 + off + 2 * kk, id, kk > 0);
-          if (elect_one()) umma_ss(tmem + C::T_DP, ddo0 + off + 2 * kk, dv0 + off + 2 * kk, id, kk > 0);
+          if (elect_one()) umma_ss(tsb, dq0 + off + 2 * kk, dk0 + off + 2 * kk, id, kk > 0);
+          if (elect_one()) umma_ss(tsb + C::T_DP, ddo0 + off + 2 * kk, dv0 + off + 2 * kk, id, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -913,11 +917,11 @@ __global__ void __launch_bounds__(384, 1)
           const uint64_t bb = BIAS_K_CONTIG
                                   ? db + ((uint32_t)(kk * 2048) >> 4)
                                   : db + ((uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-          if (elect_one()) umma_ss(tmem + C::T_S, a, bb, id_b, 1u);
+          if (elect_one()) umma_ss(tsb, a, bb, id_b, 1u);
         }
         if (elect_one()) {
           umma_commit(&bar_empty[st]);
-          umma_commit(&bar_s_full);
+          umma_commit(&bar_s_full[i & 1]);
         }
         __syncwarp();
       }
@@ -961,7 +965,7 @@ __global__ void __launch_bounds__(384, 1)
       const float nlse2 = jg < p.N ? -pre_l * kLog2e : -INFINITY;
       const float ndl = jg < p.N ? -pre_d : 0.f;
       prefetch(i + 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full, i & 1, wctx));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[i & 1], (i >> 1) & 1, wctx));
       if (!ok) break;
       tc_fence_after();
       const float2 nl = make_float2(nlse2, nlse2), nd = make_float2(ndl, ndl);
@@ -971,12 +975,13 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t sx[32], dpx[32];
-        tmem_ld32(lane_base + C::T_S + 64 * wg + 32 * half, sx);
-        tmem_ld32(lane_base + C::T_DP + 64 * wg + 32 * half, dpx);
+        const uint32_t tb = lane_base + C::T_BUF * (i & 1);
+        tmem_ld32(tb + C::T_S + 64 * wg + 32 * half, sx);
+        tmem_ld32(tb + C::T_DP + 64 * wg + 32 * half, dpx);
         tmem_wait_ld();
         if (half == 1) {  // S and dP of this s are in registers
           tc_fence_before();
-          mbar_arrive(&bar_sdp_free);
+          mbar_arrive(&bar_sdp_free[i & 1]);
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
