@@ -595,7 +595,35 @@ __global__ void __launch_bounds__(384, 1)
       return mk < p.N ? (int)p.mask[mi.b * p.msb + (int64_t)mi.s * p.mss + (int64_t)mk * p.msk] : 1;
     };
     int mask_next = mask_of(0);
-    bool ok = true;
+    // End of an item: its last dQ partial, then dK (warpgroup 0) and dV
+    // (warpgroup 1) of its key tile.  Run after the math of the next item's
+    // first tile, by which time the item's last MMAs have completed, so the
+    // compute threads never idle on them at an item boundary.
+    auto item_end = [&](const DkdvItem& e, int g_last) {
+      dq_epilogue(g_last, e.row0, njt - 1);
+      uint32_t r[D];
+      const uint32_t col = wg == 0 ? C::T_DK : C::T_DV;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c)
+        tmem_ld16(lane_base + col + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * c]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&bar_dkdv_free);
+      const int ek = e.kt * 128 + kl;
+      if (ek < p.N) {
+        __nv_bfloat16* dst = wg == 0 ? p.dk + p.sdk.at(e.b, e.s, e.h, ek, 0)
+                                     : p.dv + p.sdv.at(e.b, e.s, e.h, ek, 0);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          float f[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) f[q] = __uint_as_float(r[8 * c + q]);
+          *reinterpret_cast<uint4*>(dst + 8 * c) = pack8(f);
+        }
+      }
+    };
+    bool ok = true, pending = false;
+    DkdvItem prev{};
     int g = 0;
     for (int n = 0; n < my_items && ok; ++n) {
       const DkdvItem it = item(n);
@@ -655,6 +683,10 @@ __global__ void __launch_bounds__(384, 1)
           if (!ok) break;
           tc_fence_after();
         }
+        if (pending) {  // the previous item's last tile is g - 1
+          item_end(prev, g - 1);
+          pending = false;
+        }
         tmem_st32(lane_base + C::T_P + 32 * wg, pk);
         tmem_st32(lane_base + C::T_DS + 32 * wg, dk2);
         // dS into shared memory as the M-major A operand of dQ = dS K: row k,
@@ -672,31 +704,15 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(&bar_p_ready);
         if (jt > 0) dq_epilogue(g - 1, it.row0, jt - 1);  // its MMAs completed (waited above)
       }
-      if (!ok) break;
-      // ---- end of the item: last dQ partial, then dK (warpgroup 0) and dV
-      // (warpgroup 1) of this key tile ---------------------------------------
+      prev = it;
+      pending = true;
+    }
+    // the last item's end
+    if (ok && pending) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done, (g - 1) & 1, wctx));
-      if (!ok) break;
-      tc_fence_after();
-      dq_epilogue(g - 1, it.row0, njt - 1);
-      uint32_t r[D];
-      const uint32_t col = wg == 0 ? C::T_DK : C::T_DV;
-#pragma unroll
-      for (int c = 0; c < D / 16; ++c)
-        tmem_ld16(lane_base + col + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * c]));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bar_dkdv_free);
-      if (kg < p.N) {
-        __nv_bfloat16* dst = wg == 0 ? p.dk + p.sdk.at(it.b, it.s, it.h, kg, 0)
-                                     : p.dv + p.sdv.at(it.b, it.s, it.h, kg, 0);
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * c + e]);
-          *reinterpret_cast<uint4*>(dst + 8 * c) = pack8(f);
-        }
+      if (ok) {
+        tc_fence_after();
+        item_end(prev, g - 1);
       }
     }
     teardown();
