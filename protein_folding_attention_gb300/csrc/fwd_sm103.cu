@@ -116,8 +116,8 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_q, bar_kv_full[C::NS], bar_kv_empty[C::NS], bar_bias_full[2],
-      bar_bias_empty[2], bar_s_full[2], bar_s_free[C::NT], bar_p_ready[2], bar_o_done[C::G],
-      bar_drain[2];
+      bar_bias_empty[2], bar_s_full[C::NT], bar_s_free[C::NT], bar_p_ready[C::NT],
+      bar_o_done[C::G], bar_drain[2];
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
 
@@ -142,11 +142,16 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_bias_full[i], 1);
       mbar_init(&bar_bias_empty[i], 1);  // after the last T of a kt
-      mbar_init(&bar_s_full[i], 1);
-      mbar_init(&bar_p_ready[i], 128);
       mbar_init(&bar_drain[i], 1);
     }
-    for (int i = 0; i < C::NT; ++i) mbar_init(&bar_s_free[i], 1);
+    // T ready / P ready / buffer free, one of each per T buffer: the next
+    // completion of a buffer's barrier needs the buffer's current tile to
+    // have been consumed, so no waiter can fall two phases behind
+    for (int i = 0; i < C::NT; ++i) {
+      mbar_init(&bar_s_full[i], 1);
+      mbar_init(&bar_p_ready[i], 128);  // the warpgroup owning the tile
+      mbar_init(&bar_s_free[i], 1);
+    }
     for (int i = 0; i < C::G; ++i) mbar_init(&bar_o_done[i], 1);
     fence_barrier_init();
   }
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(384, 1)
             if (elect_one()) umma_ss(tb, a, bb, id_b, 1u);
           }
           if (elect_one()) {
-            umma_commit(&bar_s_full[s & 1]);
+            umma_commit(&bar_s_full[buf]);
             if (s == g_eff - 1) umma_commit(&bar_bias_empty[kt & 1]);
           }
           __syncwarp();
@@ -352,15 +357,13 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else {
       constexpr uint32_t id_o = idesc_bf16(128, D, 0, 1);  // P from TMEM, V MN-major
-      int np0 = 0, np1 = 0;  // tiles of each warpgroup handled so far
       for (int kt = 0, i = 0; kt < nkt && ok; ++kt) {
         for (int s = 0; s < g_eff; ++s, ++i) {
-          const int w = s & 1;
-          ok = __all_sync(0xffffffffu, mbar_wait(&bar_p_ready[w], (w ? np1 : np0) & 1, wctx));
+          const int buf = i % C::NT;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_p_ready[buf], (i / C::NT) & 1, wctx));
           if (!ok) break;
-          if (w) ++np1; else ++np0;
           tc_fence_after();
-          const int st = i % C::NS, buf = i % C::NT;
+          const int st = i % C::NS;
           const uint64_t dv = dv0 + ((uint32_t)(st * C::TILE) >> 4);
           const uint32_t o = tmem + C::TMEM_O + s * D, pa = tmem + 128 * buf;
 #pragma unroll
@@ -402,7 +405,6 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
     for (int u = 0; u < C::G / 2; ++u) { m_run[u] = -INFINITY; l_run[u] = 0.f; }
     bool ok = wg < n_wg;
-    int it = 0;  // tiles done by this warpgroup
     for (int kt = 0; kt < nkt && ok; ++kt) {
 #pragma unroll
       for (int u = 0; u < C::G / 2; ++u) {
@@ -411,7 +413,7 @@ __global__ void __launch_bounds__(384, 1)
         const int i = kt * g_eff + s;
         const int st = i % C::NS;
         const uint32_t tcol = lane_base + 128 * (i % C::NT);  // T of this tile, then P
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[wg], it & 1, wctx));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_s_full[i % C::NT], (i / C::NT) & 1, wctx));
         if (!ok) break;
         tc_fence_after();
         uint32_t x[128];
@@ -487,8 +489,7 @@ __global__ void __launch_bounds__(384, 1)
         m_run[u] = m_new;
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bar_p_ready[wg]);
-        ++it;
+        mbar_arrive(&bar_p_ready[i % C::NT]);
       }
     }
     // ---- epilogue: O / l, sigmoid gate, lse -------------------------------
