@@ -276,14 +276,42 @@ def run_ours(args, w):
         h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
         d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
+        # Copies overlap the kernels inside each step, in the order the data
+        # is needed or produced: dout (read only by the backward) goes up on a
+        # second stream while the forward runs; out comes back while the
+        # backward runs; dgate, dk and dv come back once the backward stage
+        # that writes them has finished (its stage events), dq and dbias at
+        # the end.  The step ends when every copy has landed.
+        cs = torch.cuda.Stream(dev)
+        e_dout, e_fwd = torch.cuda.Event(), torch.cuda.Event()
+        bev = [torch.cuda.Event() for _ in range(5)]
+        late = [k for k in ("dq", "dbias") if k in host_out]
+
         def e2e_step():
+            cs.wait_stream(stream)  # the previous step is done with every buffer
+            with torch.cuda.stream(cs):
+                if host_in.get("dout") is not None:
+                    x["dout"].copy_(host_in["dout"], non_blocking=True)
+                e_dout.record(cs)
             for k, v in host_in.items():
-                if v is not None:
+                if v is not None and k != "dout":
                     x[k].copy_(v, non_blocking=True)
             fwd()
-            bwd()
-            for k, v in host_out.items():
-                v.copy_(outs[k], non_blocking=True)
+            e_fwd.record(stream)
+            stream.wait_event(e_dout)
+            with torch.cuda.stream(cs):
+                cs.wait_event(e_fwd)
+                host_out["out"].copy_(outs["out"], non_blocking=True)
+            bwd(bev)
+            with torch.cuda.stream(cs):
+                cs.wait_event(bev[1])  # after k_pre: dgate
+                host_out["dgate"].copy_(outs["dgate"], non_blocking=True)
+                cs.wait_event(bev[2])  # after k_dkdv: dk, dv
+                host_out["dk"].copy_(outs["dk"], non_blocking=True)
+                host_out["dv"].copy_(outs["dv"], non_blocking=True)
+            for k in late:
+                host_out[k].copy_(outs[k], non_blocking=True)
+            stream.wait_stream(cs)
 
         e2e_step()
         barrier()
