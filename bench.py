@@ -206,10 +206,10 @@ def run_ours(args, w):
     def fwd():
         evoattn.fwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out=out, lse=lse)
 
-    def bwd(events=None):
+    def bwd(events=None, flags=evoattn.DBIAS_DETERMINISTIC):
         evoattn.bwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out, lse,
-                    x["dout"], dq=grads["dq"], dk=grads["dk"], dv=grads["dv"], dbias=dbias,
-                    dgate=grads["dgate"], workspace=wsp, stage_events=events)
+                    x["dout"], flags=flags, dq=grads["dq"], dk=grads["dk"], dv=grads["dv"],
+                    dbias=dbias, dgate=grads["dgate"], workspace=wsp, stage_events=events)
 
     def barrier():
         if pg is not None:
@@ -263,6 +263,32 @@ def run_ours(args, w):
     total_flops = (w.fwd_flops + w.bwd_flops) * ws
     value = job_tflops(w.fwd_flops + w.bwd_flops, ws, step)
     peak = peaks["bf16_tflops"]
+
+    # ---- dbias: the atomic variant timed beside the deterministic one --------
+    # (same workspace: the deterministic one needs the larger)
+    ev_a = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+            for _ in range(max(3, args.steps // 2))]
+    for _ in range(2):
+        bwd(None, evoattn.DBIAS_ATOMIC)
+    for e in ev_a:
+        bwd(e, evoattn.DBIAS_ATOMIC)
+    barrier()
+    stage_a = [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev_a) * 1e-3
+               for k in range(n_ev - 1)]
+    # HBM bytes of the deterministic reduce stage: slot partials read + dbias
+    # written (k_dbias_sum), fp32 dQ read + bf16 dq written (k_dq_convert)
+    nt = (w.N + 127) // 128
+    slots = min(w.S, max(1, -(-4 * 152 // (w.B * w.H * nt * nt))))
+    n2 = w.B * w.H * w.N * w.N
+    lin = w.B * w.S * w.H * w.N * w.D
+    reduce_bytes = (slots + 1) * n2 * 4 + lin * 4 + lin * 2
+    dbias_variants = {
+        "deterministic": {"dbias_ms": stage[2] * 1e3, "reduce_ms": stage[3] * 1e3,
+                          "bwd_ms": sum(stage) * 1e3, "slots": slots,
+                          "reduce_hbm_gbs": reduce_bytes / stage[3] / 1e9},
+        "atomic": {"dbias_ms": stage_a[2] * 1e3, "reduce_ms": stage_a[3] * 1e3,
+                   "bwd_ms": sum(stage_a) * 1e3},
+    }
 
     # ---- end to end: pinned host inputs -> device, fwd+bwd, results -> host
     e2e = None
@@ -369,6 +395,7 @@ def run_ours(args, w):
             "peak_tflops": peak, "peak_source": peak_src,
             "frac_of_peak": value / ws / peak,
             "memory": memory,
+            "dbias_variants": dbias_variants,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks.summary(),
             "gpu_launches": args.steps * 6,
