@@ -30,6 +30,9 @@ sys.path.insert(0, ROOT)
 METRIC = "EvoAttention fwd+bwd TFLOP/s and % of GB300 BF16 dense peak (N=768 triangle attn)"
 WORKLOAD = "pairformer_end_n768"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# ex2.approx.f32 results per clock per SM, microbenchmarked on GB300 (8 per
+# sub-partition); the third roofline of the path, beside HBM and tensor cores
+EX2_PER_CLK_PER_SM = 32
 
 
 def load_peaks():
@@ -290,6 +293,17 @@ def run_ours(args, w):
                    "bwd_ms": sum(stage_a) * 1e3},
     }
 
+    # ---- exponential unit: the forward, dK/dV and dbias kernels each
+    # evaluate exactly one ex2 per logit; peak = EX2_PER_CLK_PER_SM x SMs x
+    # the maximum SM clock
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    ex2_peak = EX2_PER_CLK_PER_SM * n_sm * sm_mhz * 1e6
+    sfu = {"ex2_per_clk_per_sm": EX2_PER_CLK_PER_SM, "sms": n_sm, "sm_mhz": sm_mhz,
+           "peak_ex2_per_s": ex2_peak, "logits": w.logits}
+    for name, t in (("evoattn_fwd_kernel", t_fwd), ("k_dkdv", stage[1]), ("k_dbias", stage[2])):
+        sfu[name] = {"logits_per_s": w.logits / t, "frac": w.logits / t / ex2_peak}
+
     # ---- end to end: pinned host inputs -> device, fwd+bwd, results -> host
     e2e = None
     if not args.no_e2e:
@@ -396,7 +410,7 @@ def run_ours(args, w):
             "frac_of_peak": value / ws / peak,
             "memory": memory,
             "dbias_variants": dbias_variants,
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roof, "sfu": sfu, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks.summary(),
             "gpu_launches": args.steps * 6,
         }
