@@ -60,7 +60,7 @@ inline int dbias_slots(const Problem& P) {
 }
 
 struct Workspace {
-  __nv_bfloat16* dOa;  // [B,S,H,N,D] dense
+  __nv_bfloat16* dOa;  // [B,S,H,N,D], dense in the memory order of out
   float* delta;        // [B,S,H,N]
   float* dq_acc;       // [B,S,H,N,D] dense fp32
   float* partial;      // [slots, B, H, N, N] fp32 (deterministic mode)
@@ -83,17 +83,46 @@ Workspace carve(const Problem& P, unsigned flags, void* base) {
 }
 
 // ---------------------------------------------------------------------------
-// k_pre: per row, D/8 threads of 8 features each.
+// k_pre: per row, D/8 threads of 8 features each.  Rows are walked in the
+// memory order of out (its s, h, n strides sorted), so that the loads of
+// out, dout and the gate and the stores of dgate and dOa (laid out the same
+// way) are contiguous runs whatever view the caller passes; the ending-node
+// view, with n the outermost storage axis, would otherwise make every row a
+// separate 64-byte access.
 // ---------------------------------------------------------------------------
 struct PreParams {
   int B, S, H, N, D;
   const __nv_bfloat16 *out, *dout, *gate;
-  Strides5 o, dO, g, dg;
+  Strides5 o, dO, g, dg, a;  // a: dOa
+  int walk_dim[3];           // axes (0 = s, 1 = h, 2 = n), fastest first
+  int walk_size[3];
   __nv_bfloat16* dgate;
   __nv_bfloat16* dOa;
   float* delta;
   float* dq_acc;
 };
+
+// Strides of a dense [B,S,H,N,D] array whose s, h, n axes are stored in the
+// order of the given view's strides (ties keep s, h, n order), and that
+// order, fastest axis first.
+Strides5 dense_like(const Problem& P, const Strides5& v, int (&dim)[3], int (&size)[3]) {
+  const int64_t vs[3] = {v.s, v.h, v.n};
+  const int sz[3] = {P.S, P.H, P.N};
+  int ord[3] = {0, 1, 2};
+  for (int i = 0; i < 3; ++i)  // stable insertion sort, largest stride first
+    for (int k = i; k > 0 && vs[ord[k]] > vs[ord[k - 1]]; --k) {
+      const int t = ord[k]; ord[k] = ord[k - 1]; ord[k - 1] = t;
+    }
+  int64_t st[3];
+  int64_t run = P.D;
+  for (int k = 2; k >= 0; --k) {  // innermost (smallest stride) first
+    st[ord[k]] = run;
+    run *= sz[ord[k]];
+    dim[2 - k] = ord[k];
+    size[2 - k] = sz[ord[k]];
+  }
+  return Strides5{run, st[0], st[1], st[2], 1};
+}
 
 __device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
   f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
@@ -109,15 +138,24 @@ __global__ void __launch_bounds__(256) k_pre(const PreParams p) {
   constexpr int TPR = D / 8;  // threads per row
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t rows = (int64_t)p.B * p.S * p.H * p.N;
-  const int64_t row = t / TPR;
+  const int64_t r = t / TPR;  // row in walk order
   const int part = (int)(t % TPR);
-  const bool live = row < rows;
+  const bool live = r < rows;
   float dl = 0.f;
+  int64_t row = 0;  // dense [B,S,H,N] row (delta)
   if (live) {
-    const int j = (int)(row % p.N);
-    const int h = (int)((row / p.N) % p.H);
-    const int s = (int)((row / ((int64_t)p.N * p.H)) % p.S);
-    const int b = (int)(row / ((int64_t)p.N * p.H * p.S));
+    const int i0 = (int)(r % p.walk_size[0]);
+    int64_t q = r / p.walk_size[0];
+    const int i1 = (int)(q % p.walk_size[1]);
+    q /= p.walk_size[1];
+    const int i2 = (int)(q % p.walk_size[2]);
+    const int b = (int)(q / p.walk_size[2]);
+    // axis a sits at walk position k where walk_dim[k] == a
+    auto pick = [&](int a) {
+      return p.walk_dim[0] == a ? i0 : (p.walk_dim[1] == a ? i1 : i2);
+    };
+    const int s = pick(0), h = pick(1), j = pick(2);
+    row = (((int64_t)b * p.S + s) * p.H + h) * p.N + j;
     float o[8], go[8], sg[8];
     unpack8(*reinterpret_cast<const uint4*>(p.out + p.o.at(b, s, h, j, 8 * part)), o);
     unpack8(*reinterpret_cast<const uint4*>(p.dout + p.dO.at(b, s, h, j, 8 * part)), go);
@@ -140,8 +178,10 @@ __global__ void __launch_bounds__(256) k_pre(const PreParams p) {
       dl = fmaf(go[e], o[e], dl);
       a[e] = go[e] * sg[e];
     }
-    *reinterpret_cast<uint4*>(p.dOa + row * D + 8 * part) = pack8(a);
-    float4* z = reinterpret_cast<float4*>(p.dq_acc + row * D + 8 * part);
+    *reinterpret_cast<uint4*>(p.dOa + p.a.at(b, s, h, j, 8 * part)) = pack8(a);
+    // the fp32 dQ buffer (dense) is zeroed in thread order: 32 contiguous
+    // bytes per thread
+    float4* z = reinterpret_cast<float4*>(p.dq_acc + 8 * t);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -1149,13 +1189,15 @@ template <int D, bool KC>
 cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, const Workspace& w,
                        unsigned int* status, cudaStream_t st, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const CUtensorMap& tb, cudaEvent_t* ev) {
+                       const CUtensorMap& tb, const Strides5& ado, const PreParams& walk,
+                       cudaEvent_t* ev) {
   const int nt = (P.N + 127) / 128;
   if (ev) cudaEventRecord(ev[0], st);
   // 1) delta, dgate, dOa; zero dQ accumulator
   {
-    PreParams pp{};
+    PreParams pp = walk;
     pp.B = P.B; pp.S = P.S; pp.H = P.H; pp.N = P.N; pp.D = D;
+    pp.a = ado;
     pp.out = static_cast<const __nv_bfloat16*>(a.out);
     pp.dout = static_cast<const __nv_bfloat16*>(a.dout);
     pp.gate = static_cast<const __nv_bfloat16*>(a.gate);
@@ -1237,19 +1279,19 @@ template <int D>
 cudaError_t bwd_d(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
                   unsigned int* status, cudaStream_t st, bool* tmap_ok, cudaEvent_t* ev) {
   const Workspace w = carve(P, flags, ws);
-  // dOa is written dense [B,S,H,N,D]
-  const Strides5 dense{(int64_t)P.S * P.H * P.N * D, (int64_t)P.H * P.N * D, (int64_t)P.N * D,
-                       D, 1};
+  // dOa is dense in the memory order of out
+  PreParams walk{};
+  const Strides5 ado = dense_like(P, P.o, walk.walk_dim, walk.walk_size);
   CUtensorMap tq, tk, tv, tdo, tb;
   const bool kc = P.bias.k == 1;
   if (!tmap_rows(&tq, a.q, P.q, P) || !tmap_rows(&tk, a.k, P.k, P) ||
-      !tmap_rows(&tv, a.v, P.v, P) || !tmap_rows(&tdo, w.dOa, dense, P) ||
+      !tmap_rows(&tv, a.v, P.v, P) || !tmap_rows(&tdo, w.dOa, ado, P) ||
       !tmap_bias(&tb, a.bias, P.bias, P, kc)) {
     *tmap_ok = false;
     return cudaErrorInvalidValue;
   }
-  return kc ? bwd_launch<D, true>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb, ev)
-            : bwd_launch<D, false>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb, ev);
+  return kc ? bwd_launch<D, true>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb, ado, walk, ev)
+            : bwd_launch<D, false>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb, ado, walk, ev);
 }
 
 }  // namespace
