@@ -133,61 +133,80 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                     pack_bf16(f[6], f[7]));
 }
 
-template <int D>
+// Each thread takes U units (row, 8 features) a grid apart and issues the
+// loads of all of them before the arithmetic, so more bytes are in flight.
+template <int D, int U>
 __global__ void __launch_bounds__(256) k_pre(const PreParams p) {
   constexpr int TPR = D / 8;  // threads per row
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t rows = (int64_t)p.B * p.S * p.H * p.N;
-  const int64_t r = t / TPR;  // row in walk order
-  const int part = (int)(t % TPR);
-  const bool live = r < rows;
-  float dl = 0.f;
-  int64_t row = 0;  // dense [B,S,H,N] row (delta)
-  if (live) {
-    const int i0 = (int)(r % p.walk_size[0]);
-    int64_t q = r / p.walk_size[0];
-    const int i1 = (int)(q % p.walk_size[1]);
-    q /= p.walk_size[1];
-    const int i2 = (int)(q % p.walk_size[2]);
-    const int b = (int)(q / p.walk_size[2]);
-    // axis a sits at walk position k where walk_dim[k] == a
-    auto pick = [&](int a) {
-      return p.walk_dim[0] == a ? i0 : (p.walk_dim[1] == a ? i1 : i2);
-    };
-    const int s = pick(0), h = pick(1), j = pick(2);
-    row = (((int64_t)b * p.S + s) * p.H + h) * p.N + j;
-    float o[8], go[8], sg[8];
-    unpack8(*reinterpret_cast<const uint4*>(p.out + p.o.at(b, s, h, j, 8 * part)), o);
-    unpack8(*reinterpret_cast<const uint4*>(p.dout + p.dO.at(b, s, h, j, 8 * part)), go);
-    if (p.gate) {
-      float g[8], dg[8];
-      unpack8(*reinterpret_cast<const uint4*>(p.gate + p.g.at(b, s, h, j, 8 * part)), g);
+  const int64_t T = (int64_t)gridDim.x * blockDim.x;  // a multiple of TPR
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t units = (int64_t)p.B * p.S * p.H * p.N * TPR;
+  const int part = (int)(t0 % TPR);
+  uint4 ro[U], rd[U], rg[U];
+  int bb[U], ss[U], hh[U], jj[U];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        sg[e] = 1.0f / (1.0f + ex2(-g[e] * kLog2e));
-        dg[e] = go[e] * o[e] * (1.0f - sg[e]);
-      }
-      *reinterpret_cast<uint4*>(p.dgate + p.dg.at(b, s, h, j, 8 * part)) = pack8(dg);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sg[e] = 1.0f;
+  for (int k = 0; k < U; ++k) {
+    const int64_t u = t0 + k * T;
+    if (u < units) {
+      const int64_t r = u / TPR;  // row in walk order
+      const int i0 = (int)(r % p.walk_size[0]);
+      int64_t q = r / p.walk_size[0];
+      const int i1 = (int)(q % p.walk_size[1]);
+      q /= p.walk_size[1];
+      const int i2 = (int)(q % p.walk_size[2]);
+      bb[k] = (int)(q / p.walk_size[2]);
+      // axis a sits at walk position k where walk_dim[k] == a
+      auto pick = [&](int a) {
+        return p.walk_dim[0] == a ? i0 : (p.walk_dim[1] == a ? i1 : i2);
+      };
+      ss[k] = pick(0); hh[k] = pick(1); jj[k] = pick(2);
+      ro[k] = *reinterpret_cast<const uint4*>(p.out + p.o.at(bb[k], ss[k], hh[k], jj[k], 8 * part));
+      rd[k] = *reinterpret_cast<const uint4*>(p.dout + p.dO.at(bb[k], ss[k], hh[k], jj[k], 8 * part));
+      if (p.gate)
+        rg[k] = *reinterpret_cast<const uint4*>(p.gate + p.g.at(bb[k], ss[k], hh[k], jj[k], 8 * part));
     }
-    float a[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      dl = fmaf(go[e], o[e], dl);
-      a[e] = go[e] * sg[e];
-    }
-    *reinterpret_cast<uint4*>(p.dOa + p.a.at(b, s, h, j, 8 * part)) = pack8(a);
-    // the fp32 dQ buffer (dense) is zeroed in thread order: 32 contiguous
-    // bytes per thread
-    float4* z = reinterpret_cast<float4*>(p.dq_acc + 8 * t);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, off);
-  if (live && part == 0) p.delta[row] = dl;
+  for (int k = 0; k < U; ++k) {
+    const int64_t u = t0 + k * T;
+    const bool live = u < units;
+    float dl = 0.f;
+    if (live) {
+      const int b = bb[k], s = ss[k], h = hh[k], j = jj[k];
+      float o[8], go[8], sg[8];
+      unpack8(ro[k], o);
+      unpack8(rd[k], go);
+      if (p.gate) {
+        float g[8], dg[8];
+        unpack8(rg[k], g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          sg[e] = 1.0f / (1.0f + ex2(-g[e] * kLog2e));
+          dg[e] = go[e] * o[e] * (1.0f - sg[e]);
+        }
+        *reinterpret_cast<uint4*>(p.dgate + p.dg.at(b, s, h, j, 8 * part)) = pack8(dg);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sg[e] = 1.0f;
+      }
+      float a[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        dl = fmaf(go[e], o[e], dl);
+        a[e] = go[e] * sg[e];
+      }
+      *reinterpret_cast<uint4*>(p.dOa + p.a.at(b, s, h, j, 8 * part)) = pack8(a);
+      // the fp32 dQ buffer (dense) is zeroed in unit order: 32 contiguous
+      // bytes per unit
+      float4* z = reinterpret_cast<float4*>(p.dq_acc + 8 * u);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, off);
+    if (live && part == 0)
+      p.delta[(((int64_t)bb[k] * p.S + ss[k]) * p.H + hh[k]) * p.N + jj[k]] = dl;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1204,8 +1223,9 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     pp.o = P.o; pp.dO = P.dout; pp.g = P.g; pp.dg = P.dg;
     pp.dgate = static_cast<__nv_bfloat16*>(a.dgate);
     pp.dOa = w.dOa; pp.delta = w.delta; pp.dq_acc = w.dq_acc;
-    const int64_t threads = P.rows() * (D / 8);
-    k_pre<D><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(pp);
+    constexpr int U = 2;
+    const int64_t units = P.rows() * (D / 8);
+    k_pre<D, U><<<(unsigned)((units + 256 * U - 1) / (256 * U)), 256, 0, st>>>(pp);
   }
   if (flags & EVOATTN_DBIAS_ATOMIC) {
     cudaError_t e = cudaMemsetAsync(a.dbias, 0, (size_t)P.B * P.H * P.N * P.N * 4, st);
