@@ -781,11 +781,11 @@ __global__ void __launch_bounds__(384, 1)
 // ---------------------------------------------------------------------------
 // k_dbias
 // ---------------------------------------------------------------------------
-// CTA = (b, h, query tile jt, key tile kt, s-slot).  Warps (384 threads): 0
-// producer, 1 MMA, 2-3 idle, 4-11 two compute warpgroups; a compute thread
-// owns query j (TMEM lane) and the 64 keys of its warpgroup's half.  Tensor
+// CTA = (b, h, query tile jt, key tile kt, s-slot).  Warps (640 threads): 0
+// producer, 1 MMA, 2-3 idle, 4-19 four compute warpgroups; a compute thread
+// owns query j (TMEM lane) and the 32 keys of its warpgroup's quarter.  Tensor
 // memory: S 0..127, dP 128..255 (fp32, lane =
-// query); each compute thread keeps its 64 dbias sums in registers across
+// query); each compute thread keeps its 32 dbias sums in registers across
 // the slot's s.  The bias tile is fetched once per CTA as the TMA delivers
 // it and added into every S tile by the identity-window MMAs.
 template <int D>
@@ -806,9 +806,15 @@ struct DbiasCfg : Tile<D> {
   // S and dP double-buffered: buffer b at 256 b, so the MMAs of the next s
   // run while the compute threads work on the current one
   static constexpr uint32_t T_S = 0, T_DP = 128, T_BUF = 256;
-  static constexpr int THREADS = 384;
-  static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 224;
-  static_assert(REGS_LOW * 128 + REGS_HIGH * 256 <= LAUNCH_REGS * THREADS, "register split");
+  // Four compute warpgroups, each with 32 keys of every tile: four warps per
+  // sub-partition hide the element-wise work's latencies that two could not
+  static constexpr int NWG = 4;                  // compute warpgroups
+  static constexpr int KPT = 128 / NWG;          // keys per compute thread
+  static constexpr int CH = 16;                  // keys per tensor-memory load
+  static constexpr int THREADS = 128 * (1 + NWG);
+  static constexpr int LAUNCH_REGS = 96, REGS_LOW = 64, REGS_HIGH = 104;
+  static_assert(REGS_LOW * 128 + REGS_HIGH * 128 * NWG <= LAUNCH_REGS * THREADS,
+                "register split");
 };
 
 struct DbiasParams {
@@ -823,7 +829,7 @@ struct DbiasParams {
 };
 
 template <int D, bool BIAS_K_CONTIG>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(DbiasCfg<D>::THREADS, 1)
     k_dbias(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
             const __grid_constant__ CUtensorMap tm_bias, const DbiasParams p) {
@@ -853,8 +859,14 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&bar_bias, 1);
     // a stage is empty once its MMAs completed (one commit) and both compute
     // warpgroups are done with its key mask (256 arrivals)
-    for (int i = 0; i < C::NST; ++i) { mbar_init(&bar_full[i], 1); mbar_init(&bar_empty[i], 257); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&bar_s_full[i], 1); mbar_init(&bar_sdp_free[i], 256); }
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(&bar_full[i], 1);
+      mbar_init(&bar_empty[i], 1 + 128 * C::NWG);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_s_full[i], 1);
+      mbar_init(&bar_sdp_free[i], 128 * C::NWG);
+    }
     mbar_init(&bar_drain, 1);
     fence_barrier_init();
   }
@@ -1022,10 +1034,10 @@ __global__ void __launch_bounds__(384, 1)
     const float c1 = kLog2e * rsqrtf((float)D);
     const float2 c1c1 = make_float2(c1, c1);
     bool ok = true;
-    // dbias accumulators of this thread's 64 keys, in registers across all s
-    float2 acc[32];
+    // dbias accumulators of this thread's KPT keys, in registers across all s
+    float2 acc[C::KPT / 2];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) acc[e] = make_float2(0.f, 0.f);
+    for (int e = 0; e < C::KPT / 2; ++e) acc[e] = make_float2(0.f, 0.f);
     // lse and delta of the next s are loaded while the current one computes
     float pre_l = 0.f, pre_d = 0.f;
     auto prefetch = [&](int i) {
@@ -1048,23 +1060,29 @@ __global__ void __launch_bounds__(384, 1)
       // warp-uniform: most key tiles have no masked key
       const bool masked = *reinterpret_cast<const int*>(smem + C::OFF_FLAG + st * 16) != 0;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sx[32], dpx[32];
+      for (int q = 0; q < C::KPT / C::CH; ++q) {
+        uint32_t sx[C::CH], dpx[C::CH];
         const uint32_t tb = lane_base + C::T_BUF * (i & 1);
-        tmem_ld32(tb + C::T_S + 64 * wg + 32 * half, sx);
-        tmem_ld32(tb + C::T_DP + 64 * wg + 32 * half, dpx);
+        const int k0 = C::KPT * wg + C::CH * q;  // first key of this chunk
+        if constexpr (C::CH == 32) {
+          tmem_ld32(tb + C::T_S + k0, sx);
+          tmem_ld32(tb + C::T_DP + k0, dpx);
+        } else {
+          tmem_ld16(tb + C::T_S + k0, sx);
+          tmem_ld16(tb + C::T_DP + k0, dpx);
+        }
         tmem_wait_ld();
-        if (half == 1) {  // S and dP of this s are in registers
+        if (q == C::KPT / C::CH - 1) {  // S and dP of this s are in registers
           tc_fence_before();
           mbar_arrive(&bar_sdp_free[i & 1]);
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int cc = 4 * half + c;  // keys 64*wg + 8*cc ..
+        for (int c = 0; c < C::CH / 8; ++c) {
+          const int kc = k0 + 8 * c;  // keys kc .. kc + 7
           float2 mv[4];
           if (masked) {
-            const float4 ma = *reinterpret_cast<const float4*>(madd + 64 * wg + 8 * cc);
-            const float4 mb = *reinterpret_cast<const float4*>(madd + 64 * wg + 8 * cc + 4);
+            const float4 ma = *reinterpret_cast<const float4*>(madd + kc);
+            const float4 mb = *reinterpret_cast<const float4*>(madd + kc + 4);
             mv[0] = add2(make_float2(ma.x, ma.y), nl); mv[1] = add2(make_float2(ma.z, ma.w), nl);
             mv[2] = add2(make_float2(mb.x, mb.y), nl); mv[3] = add2(make_float2(mb.z, mb.w), nl);
           } else {
@@ -1079,7 +1097,7 @@ __global__ void __launch_bounds__(384, 1)
             const float2 pr = make_float2(ex2(t.x), ex2(t.y));
             const float2 gg =
                 add2(make_float2(__uint_as_float(dpx[k2]), __uint_as_float(dpx[k2 + 1])), nd);
-            acc[16 * half + 4 * c + e] = fma2(pr, gg, acc[16 * half + 4 * c + e]);
+            acc[C::CH / 2 * q + 4 * c + e] = fma2(pr, gg, acc[C::CH / 2 * q + 4 * c + e]);
           }
         }
       }
@@ -1090,9 +1108,9 @@ __global__ void __launch_bounds__(384, 1)
       const int64_t base = ((int64_t)b * p.H + h) * p.N * p.N + (int64_t)jg * p.N;
       float* dst = p.atomic ? p.out + base : p.out + (int64_t)slot * p.B * p.H * p.N * p.N + base;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int k0 = kt * 128 + 64 * wg + 32 * half;
-        const float2* a2 = acc + 16 * half;
+      for (int hh = 0; hh < C::KPT / 32; ++hh) {
+        const int k0 = kt * 128 + C::KPT * wg + 32 * hh;
+        const float2* a2 = acc + 16 * hh;
         if (k0 + 32 <= p.N && (p.N & 3) == 0) {
 #pragma unroll
           for (int c = 0; c < 16; c += 2) {
