@@ -316,53 +316,91 @@ def run_ours(args, w):
         h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
         d2h = sum(v.numel() * v.element_size() for v in host_out.values())
 
-        # Copies overlap the kernels inside each step, in the order the data
-        # is needed or produced: dout (read only by the backward) goes up on a
-        # second stream while the forward runs; out comes back while the
-        # backward runs; dgate, dk and dv come back once the backward stage
-        # that writes them has finished (its stage events), dq and dbias at
-        # the end.  The step ends when every copy has landed.
-        cs = torch.cuda.Stream(dev)
-        e_dout, e_fwd = torch.cuda.Event(), torch.cuda.Event()
-        bev = [torch.cuda.Event() for _ in range(5)]
-        late = [k for k in ("dq", "dbias") if k in host_out]
+        # Steps are pipelined the way a training loop prefetches its next
+        # batch: two sets of device inputs and outputs alternate, so step
+        # i+1's inputs go up (stream `up`) while step i computes, and step
+        # i's results come down (stream `dn`) as soon as the kernel that
+        # writes each of them has finished (the forward's end and the
+        # backward's stage events).  Every step still uploads all of its
+        # inputs and downloads all of its results inside the timed region.
+        def make_set():
+            xs = {k: (None if v is None else torch.empty_strided(
+                v.size(), v.stride(), dtype=v.dtype, device=dev)) for k, v in x.items()}
+            ys = {"out": synthetic.empty_view(w, dev),
+                  "lse": torch.empty(B, S, H, N, device=dev, dtype=torch.float32),
+                  "dbias": torch.empty(B, H, N, N, device=dev, dtype=torch.float32)}
+            for n in ("dq", "dk", "dv", "dgate"):
+                ys[n] = synthetic.empty_view(w, dev) if grads.get(n) is not None else None
+            return xs, ys
 
-        def e2e_step():
-            cs.wait_stream(stream)  # the previous step is done with every buffer
-            with torch.cuda.stream(cs):
-                if host_in.get("dout") is not None:
-                    x["dout"].copy_(host_in["dout"], non_blocking=True)
-                e_dout.record(cs)
-            for k, v in host_in.items():
-                if v is not None and k != "dout":
-                    x[k].copy_(v, non_blocking=True)
-            fwd()
-            e_fwd.record(stream)
-            stream.wait_event(e_dout)
-            with torch.cuda.stream(cs):
-                cs.wait_event(e_fwd)
-                host_out["out"].copy_(outs["out"], non_blocking=True)
-            bwd(bev)
-            with torch.cuda.stream(cs):
-                cs.wait_event(bev[1])  # after k_pre: dgate
-                host_out["dgate"].copy_(outs["dgate"], non_blocking=True)
-                cs.wait_event(bev[2])  # after k_dkdv: dk, dv
-                host_out["dk"].copy_(outs["dk"], non_blocking=True)
-                host_out["dv"].copy_(outs["dv"], non_blocking=True)
-            for k in late:
-                host_out[k].copy_(outs[k], non_blocking=True)
-            stream.wait_stream(cs)
+        sets = [make_set(), make_set()]
+        up, dn = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        e_up = [torch.cuda.Event() for _ in range(2)]
+        e_done = [torch.cuda.Event() for _ in range(2)]
+        e_dl = [torch.cuda.Event() for _ in range(2)]
+        e_f = [torch.cuda.Event() for _ in range(2)]
+        bevs = [[torch.cuda.Event() for _ in range(5)] for _ in range(2)]
+        used = [False, False]
 
-        e2e_step()
+        def e2e_step(i):
+            sb = i % 2
+            xs, ys = sets[sb]
+            with torch.cuda.stream(up):
+                if used[sb]:
+                    up.wait_event(e_done[sb])  # step i-2 no longer reads these inputs
+                for k, v in host_in.items():
+                    if v is not None:
+                        xs[k].copy_(v, non_blocking=True)
+                e_up[sb].record(up)
+            stream.wait_event(e_up[sb])
+            if used[sb]:
+                stream.wait_event(e_dl[sb])  # step i-2's results have left these buffers
+            evoattn.fwd(xs["q"], xs["k"], xs["v"], xs["bias"], xs["mask"], xs["gate"],
+                        out=ys["out"], lse=ys["lse"])
+            e_f[sb].record(stream)
+            ev = bevs[sb]
+            evoattn.bwd(xs["q"], xs["k"], xs["v"], xs["bias"], xs["mask"], xs["gate"],
+                        ys["out"], ys["lse"], xs["dout"], dq=ys["dq"], dk=ys["dk"],
+                        dv=ys["dv"], dbias=ys["dbias"], dgate=ys["dgate"], workspace=wsp,
+                        stage_events=ev)
+            e_done[sb].record(stream)
+            with torch.cuda.stream(dn):
+                dn.wait_event(e_f[sb])
+                host_out["out"].copy_(ys["out"], non_blocking=True)
+                if "dgate" in host_out:
+                    dn.wait_event(ev[1])  # after k_pre
+                    host_out["dgate"].copy_(ys["dgate"], non_blocking=True)
+                dn.wait_event(ev[2])  # after k_dkdv
+                host_out["dk"].copy_(ys["dk"], non_blocking=True)
+                host_out["dv"].copy_(ys["dv"], non_blocking=True)
+                dn.wait_event(e_done[sb])
+                host_out["dq"].copy_(ys["dq"], non_blocking=True)
+                host_out["dbias"].copy_(ys["dbias"], non_blocking=True)
+                e_dl[sb].record(dn)
+            used[sb] = True
+
+        for i in range(2):
+            e2e_step(i)
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ksteps = max(3, args.steps // 2)
+        ksteps = max(4, args.steps // 2)
         barrier()
         e0.record(stream)
-        for _ in range(ksteps):
-            e2e_step()
+        up.wait_event(e0)
+        dn.wait_event(e0)
+        for i in range(ksteps):
+            e2e_step(i)
+        stream.wait_stream(up)
+        stream.wait_stream(dn)
         e1.record(stream)
         barrier()
+        if evoattn.device_status() != evoattn.OK:
+            raise RuntimeError("device status set during the end-to-end steps")
+        # the results that came down are the ones the device-resident steps
+        # computed from the same inputs (bit for bit: out, dk, dv, dgate)
+        for k in ("out", "dk", "dv", "dgate"):
+            if k in host_out and not torch.equal(host_out[k], outs[k].cpu()):
+                raise RuntimeError(f"end-to-end {k} differs from the device-resident result")
         te = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / ksteps, pg, dev)
         e2e = {"value": total_flops / te / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3}
