@@ -36,10 +36,12 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// No memory clobber: the kernels that reduce into a buffer never read it
+// back (a later kernel does), so the compiler may move other memory accesses
+// across these (measured ~0.6 % on k_dkdv).
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
+               "f"(c), "f"(d));
 }
 
 // ---------------------------------------------------------------------------
