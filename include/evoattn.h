@@ -30,10 +30,14 @@
  *
  * CONVENTIONS (all entry points)
  *  - Ownership: the caller owns every buffer.  Device pointers point to
- *    device memory of the current CUDA device; the library keeps no state
- *    between calls except one 4-byte device status word per device (see
- *    evoattn_get_device_status) and the cached driver entry point used to
- *    build tensor maps.  It never allocates device memory.
+ *    device memory of the current CUDA device.  The library never allocates
+ *    device memory at run time; what it holds is static: two 4-byte status
+ *    words per device (see evoattn_get_device_status), the
+ *    EVOATTN_NOALLOC_SCRATCH_BYTES array that only evoattn_bwd_noalloc uses
+ *    (held on every device that loads the library until the process exits,
+ *    shared by all calls of that entry point, which must be serialised), the
+ *    cached driver entry point used to build tensor maps, and the settings of
+ *    evoattn_debug_set_wait.
  *  - Execution: work is enqueued on `stream` (a cudaStream_t; 0 = legacy
  *    default stream) and the call returns without synchronising, except
  *    evoattn_get_device_status.  Calls on different streams may run
@@ -41,9 +45,15 @@
  *  - Errors: arguments are validated on the host before anything is
  *    enqueued; a failing call returns a non-zero evoattn_status and enqueues
  *    nothing.  A launch failure returns EVOATTN_ERR_CUDA.  The library never
- *    aborts the process.
- *  - Shapes: B, S, H, N >= 1.  BF16: D in {16, 32, 64}.  F32: D in
- *    {16, 32, 64, 128}.
+ *    aborts the process.  Every wait inside a kernel is bounded (2 s by
+ *    default); a kernel that gives up a wait stops every CTA of its own
+ *    launch, leaves its outputs undefined and sets EVOATTN_ERR_TIMEOUT in the
+ *    device status (evoattn_get_device_status).  Other launches, earlier or
+ *    later, on any stream, are not affected.
+ *  - Shapes: B, S, H, N >= 1.  BF16: D in {16, 32, 64} for the forward,
+ *    {16, 32} for the backward (evoattn_bwd, evoattn_bwd_profiled and
+ *    evoattn_bwd_noalloc return EVOATTN_ERR_UNSUPPORTED for BF16 D = 64, and
+ *    evoattn_bwd_workspace_size returns 0).  F32: D in {16, 32, 64, 128}.
  *  - Strides are in ELEMENTS (not bytes), one per logical axis, for the
  *    logical shapes:  q/k/v/gate/out/dout/dq/dk/dv/dgate  [B,S,H,N,D]  as
  *    {b, s, h, n, d};  pair_bias [B,H,N,N] as {b, h, j, k};  mask [B,S,N] as
@@ -246,6 +256,26 @@ evoattn_status evoattn_bwd_noalloc(const void* q, const int64_t q_strides[5],
  * fails, EVOATTN_ERR_INVALID_ARG if device_status is NULL.
  */
 evoattn_status evoattn_get_device_status(cudaStream_t stream, int* device_status);
+
+/*
+ * Testing hook for the bounded-wait failure path; not needed in normal use.
+ * Applies to every tcgen05 kernel enqueued after the call, on any device, by
+ * any thread of the process.
+ *
+ *  limit_ns : limit of each pipeline wait inside the kernels (0 restores the
+ *             default, 2 s).  The waits of a kernel's wind-down after a
+ *             give-up (for its own copies and MMAs already in flight) keep
+ *             the default limit.
+ *  stall    : nonzero makes the compute warps' first wait in each such
+ *             kernel wait for an event that nothing ever signals, so every
+ *             CTA gives up after limit_ns, winds down and reports
+ *             EVOATTN_ERR_TIMEOUT through evoattn_get_device_status; the
+ *             outputs of those launches are undefined.  0 restores normal
+ *             operation.
+ * Always returns EVOATTN_OK.  Not synchronised with launches already
+ * enqueued by other host threads.
+ */
+evoattn_status evoattn_debug_set_wait(unsigned long long limit_ns, int stall);
 
 /* Static, NUL-terminated English description of a status code. */
 const char* evoattn_status_string(evoattn_status status);

@@ -292,7 +292,7 @@ struct DkdvParams {
   float* dq_acc;
   __nv_bfloat16 *dk, *dv;
   Strides5 sdk, sdv;
-  unsigned int* status;
+  WaitCfg wc;
 };
 
 struct DkdvItem {
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(384, 1)
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_kv_full[2], bar_kv_empty[2], bar_qd_full[C::NQ], bar_qd_empty[C::NQ],
       bar_b_full[C::NB], bar_b_empty[C::NB], bar_s_full, bar_sdp_free, bar_p_ready,
-      bar_mma_done, bar_dq_free[2], bar_dkdv_free, bar_drain[3];
+      bar_mma_done, bar_dq_free[2], bar_dkdv_free, bar_drain[3], bar_never;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -345,6 +345,7 @@ __global__ void __launch_bounds__(384, 1)
     // dV/dK and dQ of a tile are committed by two issuers
     mbar_init(&bar_mma_done, 2); mbar_init(&bar_dkdv_free, 256);
     for (int i = 0; i < 3; ++i) mbar_init(&bar_drain[i], 1);
+    mbar_init(&bar_never, 1);  // nothing arrives: the stall test waits on it
     fence_barrier_init();
   }
   write_identity_windows(smem + C::OFF_Z, D, threadIdx.x, C::THREADS);
@@ -358,7 +359,7 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_p = &abort_flag;
-  const WaitCtx wctx{abort_p, p.status};
+  const WaitCtx wctx{abort_p, p.wc};
   auto teardown = [&]() {
     tc_fence_before();
     __syncthreads();
@@ -366,7 +367,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       tmem_dealloc(tmem, 512);
     }
-    if (threadIdx.x == 0) report_abort(abort_p, p.status);
+    if (threadIdx.x == 0) report_abort(abort_p, p.wc);
   };
 
   if (warp < 4) {
@@ -684,6 +685,7 @@ __global__ void __launch_bounds__(384, 1)
       }
     };
     bool ok = true, pending = false;
+    if (p.wc.stall) ok = __all_sync(0xffffffffu, stall_wait(&bar_never, wctx));
     DkdvItem prev{};
     int g = 0;
     for (int n = 0; n < my_items && ok; ++n) {
@@ -827,7 +829,7 @@ struct DbiasParams {
   const float* delta;
   float* out;       // partial [slots,B,H,N,N] or dbias [B,H,N,N]
   int atomic;
-  unsigned int* status;
+  WaitCfg wc;
 };
 
 template <int D, bool BIAS_K_CONTIG>
@@ -840,7 +842,7 @@ __global__ void __launch_bounds__(DbiasCfg<D>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_bias, bar_full[C::NST], bar_empty[C::NST], bar_s_full[2],
-      bar_sdp_free[2], bar_drain;
+      bar_sdp_free[2], bar_drain, bar_never;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -870,6 +872,7 @@ __global__ void __launch_bounds__(DbiasCfg<D>::THREADS, 1)
       mbar_init(&bar_sdp_free[i], 128 * C::NWG);
     }
     mbar_init(&bar_drain, 1);
+    mbar_init(&bar_never, 1);  // nothing arrives: the stall test waits on it
     fence_barrier_init();
   }
   write_identity_windows(smem + C::OFF_Z, D, threadIdx.x, C::THREADS);
@@ -883,7 +886,7 @@ __global__ void __launch_bounds__(DbiasCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort_p = &abort_flag;
-  const WaitCtx wctx{abort_p, p.status};
+  const WaitCtx wctx{abort_p, p.wc};
   auto teardown = [&]() {
     tc_fence_before();
     __syncthreads();
@@ -891,7 +894,7 @@ __global__ void __launch_bounds__(DbiasCfg<D>::THREADS, 1)
       tc_fence_after();
       tmem_dealloc(tmem, 512);
     }
-    if (threadIdx.x == 0) report_abort(abort_p, p.status);
+    if (threadIdx.x == 0) report_abort(abort_p, p.wc);
   };
 
   if (warp < 4) {
@@ -1036,6 +1039,7 @@ __global__ void __launch_bounds__(DbiasCfg<D>::THREADS, 1)
     const float c1 = kLog2e * rsqrtf((float)D);
     const float2 c1c1 = make_float2(c1, c1);
     bool ok = true;
+    if (p.wc.stall) ok = __all_sync(0xffffffffu, stall_wait(&bar_never, wctx));
     // dbias accumulators of this thread's KPT keys, in registers across all s
     float2 acc[C::KPT / 2];
 #pragma unroll
@@ -1226,7 +1230,7 @@ cudaError_t check_regs(K kern, int launch_regs) {
 
 template <int D, bool KC>
 cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, const Workspace& w,
-                       unsigned int* status, cudaStream_t st, const CUtensorMap& tq,
+                       const WaitCfg& wait, cudaStream_t st, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                        const CUtensorMap& tb, const Strides5& ado, const PreParams& walk,
                        cudaEvent_t* ev) {
@@ -1263,7 +1267,7 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     dp.mask = a.mask; dp.msb = P.mask.b; dp.mss = P.mask.s; dp.msk = P.mask.k;
     dp.lse = a.lse; dp.delta = w.delta; dp.dq_acc = w.dq_acc;
     dp.dk = static_cast<__nv_bfloat16*>(a.dk); dp.dv = static_cast<__nv_bfloat16*>(a.dv);
-    dp.sdk = P.dk; dp.sdv = P.dv; dp.status = status;
+    dp.sdk = P.dk; dp.sdv = P.dv; dp.wc = launch_wait(wait);
     auto kern = k_dkdv<D, KC>;
     cudaError_t e = set_smem(kern, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
@@ -1289,7 +1293,7 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     bp.lse = a.lse; bp.delta = w.delta;
     bp.atomic = (flags & EVOATTN_DBIAS_ATOMIC) ? 1 : 0;
     bp.out = bp.atomic ? a.dbias : w.partial;
-    bp.status = status;
+    bp.wc = launch_wait(wait);
     auto kern = k_dbias<D, KC>;
     cudaError_t e = set_smem(kern, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
@@ -1317,7 +1321,7 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
 
 template <int D>
 cudaError_t bwd_d(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
-                  unsigned int* status, cudaStream_t st, bool* tmap_ok, cudaEvent_t* ev) {
+                  const WaitCfg& wait, cudaStream_t st, bool* tmap_ok, cudaEvent_t* ev) {
   const Workspace w = carve(P, flags, ws);
   // dOa is dense in the memory order of out
   PreParams walk{};
@@ -1330,8 +1334,8 @@ cudaError_t bwd_d(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
     *tmap_ok = false;
     return cudaErrorInvalidValue;
   }
-  return kc ? bwd_launch<D, true>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb, ado, walk, ev)
-            : bwd_launch<D, false>(P, a, flags, w, status, st, tq, tk, tv, tdo, tb, ado, walk, ev);
+  return kc ? bwd_launch<D, true>(P, a, flags, w, wait, st, tq, tk, tv, tdo, tb, ado, walk, ev)
+            : bwd_launch<D, false>(P, a, flags, w, wait, st, tq, tk, tv, tdo, tb, ado, walk, ev);
 }
 
 }  // namespace
@@ -1342,11 +1346,11 @@ size_t bf16_bwd_workspace_bytes(const Problem& P, unsigned flags) {
 }
 
 cudaError_t bf16_bwd(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
-                     unsigned int* status, cudaStream_t st, bool* tmap_ok,
+                     const WaitCfg& wait, cudaStream_t st, bool* tmap_ok,
                      cudaEvent_t* events) {
   switch (P.D) {
-    case 16: return bwd_d<16>(P, a, flags, ws, status, st, tmap_ok, events);
-    case 32: return bwd_d<32>(P, a, flags, ws, status, st, tmap_ok, events);
+    case 16: return bwd_d<16>(P, a, flags, ws, wait, st, tmap_ok, events);
+    case 32: return bwd_d<32>(P, a, flags, ws, wait, st, tmap_ok, events);
   }
   return cudaErrorNotSupported;
 }

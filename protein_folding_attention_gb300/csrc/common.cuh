@@ -8,17 +8,18 @@
 #include <stdint.h>
 
 #include "evoattn.h"
+#include "layout.cuh"
 
 namespace evo {
 
 // ---------------------------------------------------------------------------
-// Bounded waits.  A wait that gives up raises the CTA's shared abort flag; the
-// kernel then winds down and ORs (1 << EVOATTN_ERR_TIMEOUT) into the device
-// status word whose address the host passes to every kernel.
+// Bounded waits.  A wait that gives up raises the CTA's shared abort flag (so
+// the CTA's other roles stop at once), ORs (1 << EVOATTN_ERR_TIMEOUT) into the
+// device status word the host reads, and writes its launch's id into the
+// device abort word, so the other CTAs of the same launch give up at their
+// next slow-path poll instead of waiting out their own limits.  A later launch
+// has another id and is not affected by an earlier give-up.
 // ---------------------------------------------------------------------------
-// A wait gives up after this many nanoseconds of %globaltimer time.
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
-
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -92,18 +93,28 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Where a bounded wait reports a give-up: the CTA's shared abort flag (so the
-// CTA's other roles stop at once) and the device status word (so every other
-// CTA of the grid gives up at its next slow-path poll instead of waiting out
-// its own limit).
+// Where a bounded wait reports a give-up.
 struct WaitCtx {
-  volatile int* abort_flag;        // shared memory
-  volatile unsigned int* status;   // global device status word (may be null)
+  volatile int* abort_flag;  // shared memory: this CTA gave up
+  WaitCfg cfg;
 };
 
-// Report a raised abort flag to the host-visible status word.
-__device__ __forceinline__ void report_abort(volatile int* abort_flag, unsigned int* status) {
-  if (*abort_flag && status) atomicOr(status, 1u << EVOATTN_ERR_TIMEOUT);
+// Record a give-up of this launch in the device words.
+__device__ __forceinline__ void raise_timeout(const WaitCfg& c) {
+  if (!c.status) return;
+  atomicOr(c.status, 1u << EVOATTN_ERR_TIMEOUT);
+  atomicExch(c.status + 1, c.launch);
+}
+
+// Has another CTA of this launch given up?
+__device__ __forceinline__ bool launch_aborted(const WaitCfg& c) {
+  return c.status && *reinterpret_cast<volatile unsigned int*>(c.status + 1) == c.launch;
+}
+
+// Report a raised abort flag to the host-visible words (once per CTA, at
+// teardown).
+__device__ __forceinline__ void report_abort(volatile int* abort_flag, const WaitCfg& c) {
+  if (*abort_flag) raise_timeout(c);
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns
@@ -118,41 +129,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   for (uint32_t n = 0;; ++n) {
     if (mbar_try_wait(a, parity)) return true;
     if (*w.abort_flag) return false;
-    if ((n & 63) == 0 && w.status && (*w.status & (1u << EVOATTN_ERR_TIMEOUT))) {
+    if ((n & 63) == 0 && launch_aborted(w.cfg)) {
       *w.abort_flag = 1;
       return false;
     }
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (globaltimer_ns() - t0 > w.cfg.limit_ns) {
       *w.abort_flag = 1;
-      if (w.status) atomicOr(const_cast<unsigned int*>(w.status), 1u << EVOATTN_ERR_TIMEOUT);
+      raise_timeout(w.cfg);
       return false;
     }
   }
 }
 
-// Progress watchdog for a polling loop: call poll() after each round that
-// made no progress; it returns false once the loop has been stuck for the
-// wait limit or another thread/CTA gave up (and reports like mbar_wait).
-struct Watchdog {
-  unsigned long long t0;
-  uint32_t n;
-  __device__ __forceinline__ void reset() { t0 = globaltimer_ns(); n = 0; }
-  __device__ __forceinline__ bool poll(const WaitCtx& w) {
-    if (*w.abort_flag) return false;
-    if ((++n & 63) == 0) {
-      if (w.status && (*w.status & (1u << EVOATTN_ERR_TIMEOUT))) {
-        *w.abort_flag = 1;
-        return false;
-      }
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        *w.abort_flag = 1;
-        if (w.status) atomicOr(const_cast<unsigned int*>(w.status), 1u << EVOATTN_ERR_TIMEOUT);
-        return false;
-      }
-    }
-    return true;
-  }
-};
+// Testing hook (WaitCfg::stall): a wait on a barrier that nothing completes,
+// which therefore gives up after the launch's wait limit.  `never` is an
+// mbarrier initialised with count 1 that no thread arrives on.
+__device__ __forceinline__ bool stall_wait(uint64_t* never, const WaitCtx& w) {
+  return mbar_wait(never, 0, w);
+}
 
 // Bounded wait used while winding down after a give-up (for copies and MMAs
 // already issued, which complete by themselves): no early exit.

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "evoattn.h"
@@ -13,15 +14,30 @@
 
 namespace evo {
 
-// One status word per device; kernels OR error bits into it.
-__device__ unsigned int g_device_status_word = 0;
+// Two words per device: [0] status bits the kernels OR into (read and cleared
+// by evoattn_get_device_status), [1] the id of the latest launch that gave up
+// a wait (the other CTAs of that launch poll it).
+__device__ unsigned int g_device_status_words[2] = {0u, 0u};
+
+namespace {
+std::atomic<unsigned int> g_launch_counter{0};
+// testing hook state (evoattn_debug_set_wait)
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitTimeoutNs};
+std::atomic<int> g_wait_stall{0};
+}  // namespace
+
+unsigned int next_launch_id() {
+  unsigned int id = ++g_launch_counter;
+  if (id == 0) id = ++g_launch_counter;  // 0 never names a launch
+  return id;
+}
 
 namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Device address of the status word of the current device (looked up once per
-// device, with that device current).
+// Device address of the status words of the current device (looked up once
+// per device, with that device current).
 unsigned int* status_word(bool* ok) {
   static unsigned int* addr[kMaxDevices] = {};
   static std::mutex mu;
@@ -33,7 +49,7 @@ unsigned int* status_word(bool* ok) {
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status_word) != cudaSuccess) {
+    if (cudaGetSymbolAddress(&p, g_device_status_words) != cudaSuccess) {
       *ok = false;
       return nullptr;
     }
@@ -47,6 +63,21 @@ bool d_supported(evoattn_dtype dt, int D) {
   if (dt == EVOATTN_BF16) return D == 16 || D == 32 || D == 64;
   if (dt == EVOATTN_F32) return D == 16 || D == 32 || D == 64 || D == 128;
   return false;
+}
+// The BF16 backward has D = 16 and D = 32 kernels only.
+bool d_supported_bwd(evoattn_dtype dt, int D) {
+  if (dt == EVOATTN_BF16) return D == 16 || D == 32;
+  return d_supported(dt, D);
+}
+
+// Wait configuration of the next launches on the current device.
+WaitCfg wait_base(unsigned int* status) {
+  WaitCfg w{};
+  w.status = status;
+  w.launch = 0;
+  w.stall = g_wait_stall.load();
+  w.limit_ns = g_wait_limit_ns.load();
+  return w;
 }
 
 bool nonneg(const int64_t* s, int n) {
@@ -84,7 +115,13 @@ using namespace evo;
 
 extern "C" {
 
-int evoattn_version(void) { return 100; }  // 0.1.0
+int evoattn_version(void) { return 200; }  // 0.2.0
+
+evoattn_status evoattn_debug_set_wait(unsigned long long limit_ns, int stall) {
+  g_wait_limit_ns.store(limit_ns == 0 ? kWaitTimeoutNs : limit_ns);
+  g_wait_stall.store(stall != 0 ? 1 : 0);
+  return EVOATTN_OK;
+}
 
 const char* evoattn_status_string(evoattn_status s) {
   switch (s) {
@@ -107,7 +144,7 @@ evoattn_status evoattn_get_device_status(cudaStream_t stream, int* device_status
   if (cudaStreamSynchronize(stream) != cudaSuccess) return EVOATTN_ERR_CUDA;
   unsigned int v = 0;
   if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return EVOATTN_ERR_CUDA;
-  if (v != 0 && cudaMemset(w, 0, sizeof(v)) != cudaSuccess) return EVOATTN_ERR_CUDA;
+  if (v != 0 && cudaMemset(w, 0, sizeof(v)) != cudaSuccess) return EVOATTN_ERR_CUDA;  // word [0] only
   *device_status = (v & (1u << EVOATTN_ERR_TIMEOUT)) ? EVOATTN_ERR_TIMEOUT : EVOATTN_OK;
   return EVOATTN_OK;
 }
@@ -161,14 +198,14 @@ evoattn_status evoattn_fwd(const void* q, const int64_t q_strides[5], const void
   a.q = q; a.k = k; a.v = v; a.bias = pair_bias; a.gate = gate; a.mask = mask;
   a.out = out; a.lse = lse;
   bool tmap_ok = true;
-  cudaError_t e = bf16_fwd(P, a, status, stream, &tmap_ok);
+  cudaError_t e = bf16_fwd(P, a, wait_base(status), stream, &tmap_ok);
   if (!tmap_ok) return EVOATTN_ERR_ALIGNMENT;
   return cuda_status(e);
 }
 
 size_t evoattn_bwd_workspace_size(int B, int S, int H, int N, int D, evoattn_dtype dtype,
                                   unsigned flags) {
-  if (B < 1 || S < 1 || H < 1 || N < 1 || !d_supported(dtype, D) || flags > 1u) return 0;
+  if (B < 1 || S < 1 || H < 1 || N < 1 || !d_supported_bwd(dtype, D) || flags > 1u) return 0;
   Problem P{};
   P.B = B; P.S = S; P.H = H; P.N = N; P.D = D;
   return dtype == EVOATTN_F32 ? f32_bwd_workspace_bytes(P) : bf16_bwd_workspace_bytes(P, flags);
@@ -199,7 +236,7 @@ static evoattn_status bwd_impl(const void* q, const int64_t q_strides[5], const 
   if (B < 1 || S < 1 || H < 1 || N < 1 || D < 1) return EVOATTN_ERR_INVALID_ARG;
   if (flags > 1u) return EVOATTN_ERR_INVALID_ARG;
   if (dtype != EVOATTN_BF16 && dtype != EVOATTN_F32) return EVOATTN_ERR_UNSUPPORTED;
-  if (!d_supported(dtype, D)) return EVOATTN_ERR_UNSUPPORTED;
+  if (!d_supported_bwd(dtype, D)) return EVOATTN_ERR_UNSUPPORTED;
   if (!nonneg(q_strides, 5) || !nonneg(k_strides, 5) || !nonneg(v_strides, 5) ||
       !nonneg(bias_strides, 4) || !nonneg(out_strides, 5) || !nonneg(dout_strides, 5) ||
       !nonneg(dq_strides, 5) || !nonneg(dk_strides, 5) || !nonneg(dv_strides, 5) ||
@@ -249,7 +286,7 @@ static evoattn_status bwd_impl(const void* q, const int64_t q_strides[5], const 
   a.dout = dout; a.out = const_cast<void*>(out); a.lse = const_cast<float*>(lse);
   a.dq = dq; a.dk = dk; a.dv = dv; a.dgate = dgate; a.dbias = dbias;
   bool tmap_ok = true;
-  cudaError_t e = bf16_bwd(P, a, flags, workspace, status, stream, &tmap_ok, events);
+  cudaError_t e = bf16_bwd(P, a, flags, workspace, wait_base(status), stream, &tmap_ok, events);
   if (!tmap_ok) return EVOATTN_ERR_ALIGNMENT;
   return cuda_status(e);
 }

@@ -102,7 +102,7 @@ struct FwdParams {
   __nv_bfloat16* out;
   Strides5 o;
   float* lse;
-  unsigned int* status;
+  WaitCfg wc;
 };
 
 template <int D, bool BIAS_K_CONTIG, bool HAS_GATE>
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(384, 1)
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_q, bar_kv_full[C::NS], bar_kv_empty[C::NS], bar_bias_full[2],
       bar_bias_empty[2], bar_s_full[C::NT], bar_s_free[C::NT], bar_p_ready[C::NT],
-      bar_o_done[C::G], bar_drain[2];
+      bar_o_done[C::G], bar_drain[2], bar_never;
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
 
@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bar_s_free[i], 1);
     }
     for (int i = 0; i < C::G; ++i) mbar_init(&bar_o_done[i], 1);
+    mbar_init(&bar_never, 1);  // nothing arrives: the stall test waits on it
     fence_barrier_init();
   }
   // Z in the 32-byte-swizzled K-major layout the MMA reads: row r holds 16
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_slot;
   volatile int* abort_p = &abort_flag;
-  const WaitCtx wctx{abort_p, p.status};
+  const WaitCtx wctx{abort_p, p.wc};
 
   // Every role ends here: all MMAs and TMEM traffic are done once every
   // thread has arrived, then the allocating warp frees the tensor memory.
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    if (threadIdx.x == 0) report_abort(abort_p, p.status);
+    if (threadIdx.x == 0) report_abort(abort_p, p.wc);
   };
   if (warp < 4) {
   // setmaxnreg is warpgroup-aligned: one instance for warps 0-3, one for 4-11
@@ -405,6 +406,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
     for (int u = 0; u < C::G / 2; ++u) { m_run[u] = -INFINITY; l_run[u] = 0.f; }
     bool ok = wg < n_wg;
+    if (ok && p.wc.stall) ok = __all_sync(0xffffffffu, stall_wait(&bar_never, wctx));
     for (int kt = 0; kt < nkt && ok; ++kt) {
 #pragma unroll
       for (int u = 0; u < C::G / 2; ++u) {
@@ -600,7 +602,7 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 }
 
 template <int D>
-cudaError_t fwd_d(const Problem& P, const Bf16Ptrs& a, unsigned int* status, cudaStream_t st,
+cudaError_t fwd_d(const Problem& P, const Bf16Ptrs& a, const WaitCfg& wait, cudaStream_t st,
                   bool* tmap_ok) {
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv, tb;
@@ -622,7 +624,7 @@ cudaError_t fwd_d(const Problem& P, const Bf16Ptrs& a, unsigned int* status, cud
   fp.out = static_cast<__nv_bfloat16*>(a.out);
   fp.o = P.o;
   fp.lse = a.lse;
-  fp.status = status;
+  fp.wc = launch_wait(wait);
   const uint64_t grid64 = (uint64_t)fp.n_jt * P.H * fp.n_sg * P.B;
   if (grid64 > 0x7FFFFFFFull) return cudaErrorInvalidConfiguration;
   const unsigned grid = (unsigned)grid64;
@@ -635,12 +637,12 @@ cudaError_t fwd_d(const Problem& P, const Bf16Ptrs& a, unsigned int* status, cud
 
 }  // namespace
 
-cudaError_t bf16_fwd(const Problem& P, const Bf16Ptrs& a, unsigned int* status,
+cudaError_t bf16_fwd(const Problem& P, const Bf16Ptrs& a, const WaitCfg& wait,
                      cudaStream_t st, bool* tmap_ok) {
   switch (P.D) {
-    case 16: return fwd_d<16>(P, a, status, st, tmap_ok);
-    case 32: return fwd_d<32>(P, a, status, st, tmap_ok);
-    case 64: return fwd_d<64>(P, a, status, st, tmap_ok);
+    case 16: return fwd_d<16>(P, a, wait, st, tmap_ok);
+    case 32: return fwd_d<32>(P, a, wait, st, tmap_ok);
+    case 64: return fwd_d<64>(P, a, wait, st, tmap_ok);
   }
   return cudaErrorInvalidValue;
 }

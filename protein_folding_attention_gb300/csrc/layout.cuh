@@ -34,6 +34,19 @@ struct Problem {
   __host__ __device__ int64_t rows() const { return (int64_t)B * S * H * N; }
 };
 
+// Default limit of a pipeline wait, in nanoseconds of %globaltimer time.  The
+// waits of the wind-down after a give-up always use this limit.
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
+
+// Per-launch configuration of the bounded waits of a tcgen05 kernel, passed
+// by value in its parameters (see common.cuh).
+struct WaitCfg {
+  unsigned int* status;         // device words: [0] status bits, [1] abort word
+  unsigned int launch;          // this launch's id (never 0)
+  int stall;                    // testing: the compute warps' first wait never completes
+  unsigned long long limit_ns;  // limit of every pipeline wait
+};
+
 // The additive logit offset that a masked key receives.
 constexpr float kMaskBias = -1.0e9f;
 

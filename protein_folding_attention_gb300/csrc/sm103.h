@@ -17,16 +17,27 @@ struct Bf16Ptrs {
   float* dbias;
 };
 
-// Returns cudaSuccess or the first launch / tensor-map error.  `status` is the
-// device status word.  `tmap_ok` is set false when the driver rejected a
-// tensor map (alignment or size).
-cudaError_t bf16_fwd(const Problem& P, const Bf16Ptrs& a, unsigned int* status,
+// A fresh id for the next kernel launch (never 0).
+unsigned int next_launch_id();
+
+// The wait configuration of one launch: `base` with a fresh launch id.
+inline WaitCfg launch_wait(const WaitCfg& base) {
+  WaitCfg c = base;
+  c.launch = next_launch_id();
+  return c;
+}
+
+// Returns cudaSuccess or the first launch / tensor-map error.  `wait` holds
+// the device status words and the wait limit (its launch id is replaced per
+// launch).  `tmap_ok` is set false when the driver rejected a tensor map
+// (alignment or size).
+cudaError_t bf16_fwd(const Problem& P, const Bf16Ptrs& a, const WaitCfg& wait,
                      cudaStream_t st, bool* tmap_ok);
 
 size_t bf16_bwd_workspace_bytes(const Problem& P, unsigned flags);
 // `events` (nullable): 5 caller-owned events recorded around the stages.
 cudaError_t bf16_bwd(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,
-                     unsigned int* status, cudaStream_t st, bool* tmap_ok,
+                     const WaitCfg& wait, cudaStream_t st, bool* tmap_ok,
                      cudaEvent_t* events);
 
 }  // namespace evo

@@ -60,6 +60,8 @@ def load(path: str = LIB_PATH):
     lib.evoattn_status_string.restype = ctypes.c_char_p
     lib.evoattn_version.argtypes = []
     lib.evoattn_version.restype = i
+    lib.evoattn_debug_set_wait.argtypes = [ctypes.c_ulonglong, i]
+    lib.evoattn_debug_set_wait.restype = i
     _lib = lib
     return lib
 
@@ -175,6 +177,14 @@ def bwd(q, k, v, pair_bias, mask, gate, out, lse, dout, flags=DBIAS_DETERMINISTI
         st = lib.evoattn_bwd_profiled(*args, handles)
     _check(st, "evoattn_bwd")
     return {"dq": dq, "dk": dk, "dv": dv, "dbias": dbias, "dgate": dgate}
+
+
+def debug_set_wait(limit_ns: int = 0, stall: bool = False) -> None:
+    """Testing hook (evoattn_debug_set_wait): the wait limit of the kernels
+    enqueued from now on (0 = the default 2 s) and whether their compute warps'
+    first wait stalls until it gives up."""
+    _check(load().evoattn_debug_set_wait(int(limit_ns), 1 if stall else 0),
+           "evoattn_debug_set_wait")
 
 
 def device_status(stream=None) -> int:

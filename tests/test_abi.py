@@ -113,6 +113,38 @@ def test_bwd_rejects_bad_arguments(lib):
     assert call_bwd(lib, shape=(1, 4, 2, 64, 24)) == evoattn.ERR_UNSUPPORTED
 
 
+def call_bwd_noalloc(lib, *, shape=(1, 4, 2, 64, 32), dtype=evoattn.BF16, flags=0):
+    B, S, H, N, D = shape
+    s = dense5(*shape)
+    bs = S4(H * N * N, N * N, N, 1)
+    fn = lib.evoattn_bwd_noalloc
+    fn.argtypes = lib.evoattn_bwd.argtypes[:-3] + [ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn(FAKE, s, FAKE, s, FAKE, s, FAKE, bs, None, None, None, s, FAKE, s,
+              FAKE, FAKE, s, FAKE, s, FAKE, s, FAKE, s, FAKE, None, s,
+              B, S, H, N, D, dtype, flags, None)
+
+
+def test_bf16_backward_d64_is_unsupported(lib):
+    """The BF16 forward takes D = 64, the BF16 backward does not: every
+    backward entry point says so with ERR_UNSUPPORTED (not a CUDA or
+    workspace error), and the workspace query returns 0."""
+    shape = (1, 4, 2, 64, 64)
+    assert call_bwd(lib, shape=shape) == evoattn.ERR_UNSUPPORTED
+    assert call_bwd(lib, shape=shape, flags=1) == evoattn.ERR_UNSUPPORTED
+    assert call_bwd_noalloc(lib, shape=shape) == evoattn.ERR_UNSUPPORTED
+    assert evoattn.workspace_size(1, 4, 2, 64, 64) == 0
+    # fp32 inputs have a D = 64 backward
+    assert evoattn.workspace_size(1, 4, 2, 64, 64, torch_f32()) > 0
+    # the forward accepts BF16 D = 64 (validation passes up to the alignment checks)
+    assert call_fwd(lib, shape=shape, q=ctypes.c_void_p((1 << 20) + 8)) == evoattn.ERR_ALIGNMENT
+
+
+def test_debug_wait_hook_round_trips(lib):
+    assert lib.evoattn_debug_set_wait(50_000, 1) == evoattn.OK
+    assert lib.evoattn_debug_set_wait(0, 0) == evoattn.OK
+
+
 def test_workspace_is_linear_not_cubic(lib):
     for dt in (torch_bf16(), torch_f32()):
         small = evoattn.workspace_size(1, 64, 4, 256, 32, dt)

@@ -72,6 +72,23 @@ def test_bf16_bwd_small(S, N, H, D, node, mask, gate, flags):
     check_bwd(x, run_fwd_bwd(x, flags), GRAD_REL)
 
 
+@pytest.mark.parametrize("bias_std", [8.0, 12.0])
+def test_bf16_bwd_large_pair_bias(bias_std):
+    """Gradients with a pair bias of standard deviation 8-12 (the bias term
+    dominates the logits), both bias layouts.  The softmax is then nearly one
+    key per row and dS = P (dP - delta) cancels: the bf16 rounding of out
+    (which delta is computed from) and of the gated output gradient (an MMA
+    operand) bring the gradients' relative L2 error to about 8e-3 at standard
+    deviation 12 and 1e-2 at 16 (a float64 emulation of those roundings gives
+    the same figures), so the sweep stops at 12."""
+    for node in ("starting", "ending"):
+        w = synthetic.small("lb", B=1, S=5, N=200, H=2, D=32, dtype="bf16", node=node,
+                            mask="tail", mask_tail=13, gate=True, bias_std=bias_std,
+                            seed=int(bias_std) * 10 + (node == "ending"))
+        x = synthetic.make_inputs(w)
+        check_bwd(x, run_fwd_bwd(x), GRAD_REL)
+
+
 def test_bf16_bwd_batch2():
     w = synthetic.small("b2", B=2, S=4, N=160, H=2, D=32, dtype="bf16", node="starting",
                         mask="bernoulli", mask_p=0.3, gate=True, seed=78)
@@ -104,6 +121,41 @@ def test_gradients_are_bit_identical_run_to_run():
     for k in ("dk", "dv", "dgate", "dbias"):
         assert torch.equal(a[k].view(torch.int16 if a[k].element_size() == 2 else torch.int32),
                            b[k].view(torch.int16 if b[k].element_size() == 2 else torch.int32)), k
+
+
+def _full_size_all_rows(name, flags):
+    """Every gradient of a full-size workload, over every s row, against the
+    oracle, in the benchmark's launch configuration.  This covers the
+    production s-slot walk of the dbias reduction (several slots of many s
+    rows each) element by element."""
+    w = synthetic.WORKLOADS[name]
+    xd = synthetic.make_inputs(w, device=DEV)
+    out, lse = evoattn.fwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], xd["gate"])
+    g = evoattn.bwd(xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], xd["gate"], out, lse,
+                    xd["dout"], flags=flags)
+    assert evoattn.device_status() == evoattn.OK
+    host = {k: (None if v is None else v.cpu()) for k, v in xd.items()}
+    del xd
+    ref = oracle.bwd(host["q"], host["k"], host["v"], host["bias"], host["mask"], host["gate"],
+                     host["dout"])
+    errs = {n: rel_l2(g[n], ref[n]) for n in GRADS if ref[n] is not None}
+    bad = {n: e for n, e in errs.items() if e > GRAD_REL}
+    assert not bad, f"{name}: rel-L2 over {GRAD_REL}: {errs}"
+
+
+@pytest.mark.parametrize("name", ["pairformer_start_n384", "msa_row_s512_n384"])
+def test_bf16_bwd_full_size_every_row(name):
+    _full_size_all_rows(name, evoattn.DBIAS_DETERMINISTIC)
+
+
+@pytest.mark.slow
+def test_bf16_bwd_full_size_every_row_end_n768():
+    """The benchmark workload itself (about a minute of oracle time)."""
+    _full_size_all_rows("pairformer_end_n768", evoattn.DBIAS_DETERMINISTIC)
+
+
+def test_bf16_bwd_full_size_every_row_atomic_dbias():
+    _full_size_all_rows("pairformer_start_n384", evoattn.DBIAS_ATOMIC)
 
 
 @pytest.mark.parametrize("name", ["pairformer_start_n384", "pairformer_end_n768",

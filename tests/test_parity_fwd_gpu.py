@@ -24,8 +24,8 @@ def check_fwd(x, out, lse, rel=FWD_REL, abs_=FWD_ABS):
     r, a = rel_l2(out, ref_out), max_abs(out, ref_out)
     assert np.isfinite(as_np(out)).all()
     assert r <= rel and a <= abs_, f"out rel-L2 {r:.3e} max-abs {a:.3e}"
-    rl = rel_l2(lse, ref_lse)
-    assert rl <= rel, f"lse rel-L2 {rl:.3e}"
+    rl, al = rel_l2(lse, ref_lse), max_abs(lse, ref_lse)
+    assert rl <= rel and al <= abs_, f"lse rel-L2 {rl:.3e} max-abs {al:.3e}"
     return r, a
 
 
@@ -57,6 +57,20 @@ def test_bf16_fwd_small(S, N, H, D, node, mask, gate):
     x = synthetic.make_inputs(w)
     out, lse = run_fwd(x)
     check_fwd(x, out, lse)
+
+
+@pytest.mark.parametrize("bias_std", [8.0, 16.0])
+def test_bf16_fwd_large_pair_bias(bias_std):
+    """A pair bias of standard deviation 8-16 makes the bias dominate the
+    logits, so any error in the coefficient with which it enters the logit
+    tile grows in proportion; both layouts of the bias tile are covered."""
+    for node in ("starting", "ending"):
+        w = synthetic.small("lb", B=1, S=3, N=200, H=2, D=32, dtype="bf16", node=node,
+                            mask="tail", mask_tail=13, gate=True, bias_std=bias_std,
+                            seed=int(bias_std) * 10 + (node == "ending"))
+        x = synthetic.make_inputs(w)
+        out, lse = run_fwd(x)
+        check_fwd(x, out, lse)
 
 
 def test_bf16_fwd_batch2():
@@ -98,4 +112,5 @@ def test_bf16_fwd_full_size_sampled(name):
                                       sl(xd["mask"]), sl(xd["gate"]))
         r, a = rel_l2(out[:, s:s + 1], ref_out), max_abs(out[:, s:s + 1], ref_out)
         assert r <= FWD_REL and a <= FWD_ABS, f"s={s}: rel {r:.3e} abs {a:.3e}"
-        assert rel_l2(lse[:, s:s + 1], ref_lse) <= FWD_REL
+        rl, al = rel_l2(lse[:, s:s + 1], ref_lse), max_abs(lse[:, s:s + 1], ref_lse)
+        assert rl <= FWD_REL and al <= FWD_ABS, f"s={s}: lse rel {rl:.3e} abs {al:.3e}"

@@ -1,0 +1,76 @@
+"""The bounded-wait failure path of the tcgen05 kernels, on the GPU, without a
+fault or a hang: the testing hook evoattn_debug_set_wait makes the compute
+warps' first wait in every kernel wait for an event that nothing signals,
+with a limit of 50 microseconds.  Each CTA must then give up, let the copies
+and MMAs it already issued finish, free its tensor memory and exit; the
+device status must read EVOATTN_ERR_TIMEOUT; and the next normal call in the
+same process must run and match the oracle (the context stays usable and the
+earlier give-up does not leak into later launches)."""
+import pytest
+import torch
+
+import oracle
+from protein_folding_attention_gb300 import evoattn, synthetic
+
+from helpers import FWD_REL, GRAD_REL, rel_l2, to_device
+
+pytestmark = pytest.mark.gpu
+
+LIMIT_NS = 50_000
+
+
+def _inputs(node):
+    w = synthetic.small("to", B=1, S=6, N=200, H=2, D=32, dtype="bf16", node=node,
+                        mask="tail", mask_tail=11, gate=True, seed=314)
+    x = synthetic.make_inputs(w)
+    return x, {k: to_device(v, "cuda") for k, v in x.items()}
+
+
+def _stalled(fn):
+    assert evoattn.device_status() == evoattn.OK
+    evoattn.debug_set_wait(LIMIT_NS, stall=True)
+    try:
+        fn()
+        status = evoattn.device_status()
+    finally:
+        evoattn.debug_set_wait(0, stall=False)
+    return status
+
+
+@pytest.mark.parametrize("node", ["starting", "ending"])
+def test_forward_gives_up_and_recovers(node):
+    x, xd = _inputs(node)
+    args = (xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], xd["gate"])
+    assert _stalled(lambda: evoattn.fwd(*args)) == evoattn.ERR_TIMEOUT
+    out, lse = evoattn.fwd(*args)
+    assert evoattn.device_status() == evoattn.OK
+    ref_out, ref_lse = oracle.fwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"])
+    assert rel_l2(out, ref_out) <= FWD_REL
+    assert rel_l2(lse, ref_lse) <= FWD_REL
+
+
+@pytest.mark.parametrize("flags", [evoattn.DBIAS_DETERMINISTIC, evoattn.DBIAS_ATOMIC])
+def test_backward_gives_up_and_recovers(flags):
+    x, xd = _inputs("ending")
+    args = (xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], xd["gate"])
+    out, lse = evoattn.fwd(*args)
+    assert evoattn.device_status() == evoattn.OK
+    status = _stalled(lambda: evoattn.bwd(*args, out, lse, xd["dout"], flags=flags))
+    assert status == evoattn.ERR_TIMEOUT
+    g = evoattn.bwd(*args, out, lse, xd["dout"], flags=flags)
+    assert evoattn.device_status() == evoattn.OK
+    ref = oracle.bwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], x["dout"])
+    for n in ("dq", "dk", "dv", "dbias", "dgate"):
+        assert torch.isfinite(g[n]).all(), n
+        assert rel_l2(g[n], ref[n]) <= GRAD_REL, n
+
+
+def test_default_limit_is_restored():
+    """After the stalled launches, a default-limit call on a full tile set
+    completes normally (no launch aborts on an earlier launch's give-up)."""
+    x, xd = _inputs("starting")
+    args = (xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], xd["gate"])
+    assert _stalled(lambda: evoattn.fwd(*args)) == evoattn.ERR_TIMEOUT
+    for _ in range(3):
+        evoattn.fwd(*args)
+    assert evoattn.device_status() == evoattn.OK

@@ -29,7 +29,7 @@ def _noalloc_fn():
     return fn
 
 
-def _call_noalloc(fn, x, out, lse, grads, dbias):
+def _call_noalloc(fn, x, out, lse, grads, dbias, flags=evoattn.DBIAS_DETERMINISTIC):
     s5 = lambda t: None if t is None else (ctypes.c_int64 * 5)(*t.stride())
     p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
     B, S, H, N, D = x["q"].shape
@@ -40,29 +40,71 @@ def _call_noalloc(fn, x, out, lse, grads, dbias):
               p(x["dout"]), s5(x["dout"]), p(grads["dq"]), s5(grads["dq"]),
               p(grads["dk"]), s5(grads["dk"]), p(grads["dv"]), s5(grads["dv"]), p(dbias),
               p(grads["dgate"]), s5(grads["dgate"]), B, S, H, N, D, evoattn.BF16,
-              evoattn.DBIAS_DETERMINISTIC,
-              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+              flags, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+def _problem(node, S, N, seed):
+    w = synthetic.small("na", B=1, S=S, N=N, H=2, D=32, dtype="bf16", node=node,
+                        mask="bernoulli", mask_p=0.2, gate=True, seed=seed)
+    assert evoattn.workspace_size(w.B, w.S, w.H, w.N, w.D) <= SCRATCH_BYTES
+    x = {k: to_device(v, "cuda") for k, v in synthetic.make_inputs(w).items()}
+    out, lse = evoattn.fwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"])
+    return x, out, lse
+
+
+def _noalloc_grads(fn, x, out, lse, flags):
+    grads = {n: torch.full_like(x["q"], float("nan")) for n in ("dq", "dk", "dv", "dgate")}
+    B, S, H, N, D = x["q"].shape
+    dbias = torch.full((B, H, N, N), float("nan"), device="cuda")
+    assert _call_noalloc(fn, x, out, lse, grads, dbias, flags) == evoattn.OK
+    assert evoattn.device_status() == evoattn.OK
+    grads["dbias"] = dbias
+    return grads
+
+
+def _bits(t):
+    return t.view(torch.int16 if t.element_size() == 2 else torch.int32)
 
 
 @pytest.mark.parametrize("node", ["starting", "ending"])
 def test_noalloc_matches_workspace_backward_twice(node):
-    w = synthetic.small("na", B=1, S=16, N=200, H=2, D=32, dtype="bf16", node=node,
-                        mask="bernoulli", mask_p=0.2, gate=True, seed=21)
-    assert evoattn.workspace_size(w.B, w.S, w.H, w.N, w.D) <= SCRATCH_BYTES
-    x = {k: to_device(v, "cuda") for k, v in synthetic.make_inputs(w).items()}
-    out, lse = evoattn.fwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"])
+    """Two calls in a row, each after the shared scratch was left dirty by a
+    different problem (other seed, other N and S, so another dbias slot
+    count and layout).  dk, dv, dgate and the deterministic dbias come from
+    the same kernels in the same order as with a caller workspace, so they
+    must agree bit for bit; a kernel that read a scratch byte it had not
+    written would break that.  dq is summed with fp32 atomics (order not
+    fixed) and is compared by relative L2 error."""
+    fn = _noalloc_fn()
+    x, out, lse = _problem(node, S=16, N=200, seed=21)
     ref = evoattn.bwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out, lse,
                       x["dout"])
-    fn = _noalloc_fn()
+    other, o_out, o_lse = _problem(node, S=24, N=256, seed=5)
     for _ in range(2):
-        grads = {n: torch.full_like(x["q"], float("nan")) for n in ("dq", "dk", "dv", "dgate")}
-        dbias = torch.full_like(ref["dbias"], float("nan"))
-        assert _call_noalloc(fn, x, out, lse, grads, dbias) == evoattn.OK
-        assert evoattn.device_status() == evoattn.OK
-        for n in ("dq", "dk", "dv", "dgate"):
-            assert torch.isfinite(grads[n]).all()
-            assert rel_l2(grads[n], ref[n]) <= GRAD_REL, n
-        assert rel_l2(dbias, ref["dbias"]) <= GRAD_REL
+        _noalloc_grads(fn, other, o_out, o_lse, evoattn.DBIAS_DETERMINISTIC)  # dirty scratch
+        g = _noalloc_grads(fn, x, out, lse, evoattn.DBIAS_DETERMINISTIC)
+        for n in ("dk", "dv", "dgate", "dbias"):
+            assert torch.equal(_bits(g[n]), _bits(ref[n])), n
+        assert torch.isfinite(g["dq"]).all()
+        assert rel_l2(g["dq"], ref["dq"]) <= GRAD_REL
+
+
+def test_noalloc_atomic_dbias_twice():
+    """The atomic dbias variant through the no-alloc entry point, twice, after
+    dirtying the scratch: dk, dv, dgate bit for bit, dbias and dq within the
+    rounding of a different summation order."""
+    fn = _noalloc_fn()
+    x, out, lse = _problem("starting", S=16, N=200, seed=22)
+    ref = evoattn.bwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out, lse,
+                      x["dout"])
+    other, o_out, o_lse = _problem("ending", S=24, N=256, seed=6)
+    for _ in range(2):
+        _noalloc_grads(fn, other, o_out, o_lse, evoattn.DBIAS_DETERMINISTIC)
+        g = _noalloc_grads(fn, x, out, lse, evoattn.DBIAS_ATOMIC)
+        for n in ("dk", "dv", "dgate"):
+            assert torch.equal(_bits(g[n]), _bits(ref[n])), n
+        assert rel_l2(g["dbias"], ref["dbias"]) <= 1e-5
+        assert rel_l2(g["dq"], ref["dq"]) <= GRAD_REL
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
