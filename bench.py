@@ -129,6 +129,84 @@ def config_block(w):
             "parallelism": "replicas", "l2": "inputs larger than L2 (no flush needed)"}
 
 
+PER_CONFIG = ("pairformer_start_n384", "pairformer_end_n768", "msa_row_s512_n384",
+              "long_start_n1536")
+
+
+def measure_config(w, dev, peak, steps=5, warmup=3):
+    """Forward and backward of one workload on its own inputs: CUDA-event
+    times (median over `steps`), TFLOP/s, fraction of the bf16 peak, and the
+    device bytes the caller holds for the call (inputs, outputs and the
+    backward workspace: the library allocates nothing itself).  Returns a
+    dict; every tensor it allocated is freed on return."""
+    import torch
+
+    from protein_folding_attention_gb300 import evoattn, synthetic
+    torch.cuda.synchronize(dev)
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    x = synthetic.make_inputs(w, device=dev)
+    B, S, H, N, D = w.B, w.S, w.H, w.N, w.D
+    out = synthetic.empty_view(w, dev)
+    lse = torch.empty(B, S, H, N, device=dev, dtype=torch.float32)
+    g = {n: synthetic.empty_view(w, dev) for n in ("dq", "dk", "dv")}
+    g["dgate"] = synthetic.empty_view(w, dev) if w.gate else None
+    dbias = torch.empty(B, H, N, N, device=dev, dtype=torch.float32)
+    wsp = torch.empty(evoattn.workspace_size(B, S, H, N, D, w.torch_dtype), device=dev,
+                      dtype=torch.uint8)
+
+    def fwd():
+        evoattn.fwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out=out, lse=lse)
+
+    def bwd(ev=None):
+        evoattn.bwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out, lse,
+                    x["dout"], dq=g["dq"], dk=g["dk"], dv=g["dv"], dbias=dbias,
+                    dgate=g["dgate"], workspace=wsp, stage_events=ev)
+
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    ef = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    eb = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    for i in range(steps):
+        ef[i][0].record()
+        fwd()
+        ef[i][1].record()
+        bwd(eb[i])
+    torch.cuda.synchronize(dev)
+    if evoattn.device_status() != evoattn.OK:
+        raise RuntimeError(f"device status set on {w.name}")
+    t_f = statistics.median(a.elapsed_time(b) for a, b in ef) * 1e-3
+    t_b = statistics.median(e[0].elapsed_time(e[4]) for e in eb) * 1e-3
+    held = int(torch.cuda.max_memory_allocated(dev) - base)
+    res = {"fwd_ms": t_f * 1e3, "fwd_tflops": w.fwd_flops / t_f / 1e12,
+           "fwd_frac_of_peak": w.fwd_flops / t_f / 1e12 / peak,
+           "bwd_ms": t_b * 1e3, "bwd_tflops": w.bwd_flops / t_b / 1e12,
+           "bwd_frac_of_peak": w.bwd_flops / t_b / 1e12 / peak,
+           "L": w.B * w.S * w.H * w.N * w.D, "BHN2": w.B * w.H * w.N * w.N,
+           "device_bytes": held, "bwd_workspace_bytes": int(wsp.numel()),
+           "logits_bytes_if_materialized_bf16": int(w.logits * 2)}
+    del x, out, lse, g, dbias, wsp
+    torch.cuda.synchronize(dev)
+    return res
+
+
+def memory_fit(points):
+    """Least-squares fit of device bytes = a*L + b*BHN2 + c over the given
+    {"L", "BHN2", "device_bytes"} points (L = B*S*H*N*D, BHN2 = B*H*N*N).
+    Returns the coefficients and the largest relative residual."""
+    import numpy as np
+    A = np.array([[p["L"], p["BHN2"], 1.0] for p in points], dtype=np.float64)
+    y = np.array([p["device_bytes"] for p in points], dtype=np.float64)
+    coef, *_ = np.linalg.lstsq(A, y, rcond=None)
+    resid = A @ coef - y
+    return {"bytes_per_L": float(coef[0]), "bytes_per_BHN2": float(coef[1]),
+            "const_bytes": float(coef[2]),
+            "max_rel_residual": float(np.max(np.abs(resid) / y)),
+            "points": len(points)}
+
+
 def oracle_sample_time(w, n_rows, device_inputs=None):
     """Time the float64 oracle (fwd + bwd) on n_rows of the workload's s rows.
     Returns (seconds, flops_of_sample, threads)."""
@@ -425,6 +503,14 @@ def run_ours(args, w):
         roof = {"kernel": dom, "bound": "alu", "achieved": None, "peak": None,
                 "unit": None, "frac": None, "traffic": traffic}
 
+    # ---- every synthetic configuration: fwd / bwd times and held memory ----
+    per_config = None
+    if rank == 0 and not args.no_per_config:
+        per_config = {}
+        for name in PER_CONFIG:
+            per_config[name] = measure_config(synthetic.WORKLOADS[name], dev, peak)
+        per_config["memory_fit"] = memory_fit([per_config[n] for n in PER_CONFIG])
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         dt, fl, thr = oracle_sample_time(w, args.cpu_rows)
@@ -449,6 +535,7 @@ def run_ours(args, w):
             "memory": memory,
             "dbias_variants": dbias_variants,
             "roofline": roof, "sfu": sfu, "cpu_baseline": cpu, "e2e": e2e,
+            "per_config": per_config,
             "clocks": clocks.summary(),
             "gpu_launches": args.steps * 6,
         }
@@ -488,6 +575,7 @@ def main():
                     help="profiling only: truncate the workload to this many s rows")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")

@@ -258,6 +258,37 @@ evoattn_status evoattn_bwd_noalloc(const void* q, const int64_t q_strides[5],
 evoattn_status evoattn_get_device_status(cudaStream_t stream, int* device_status);
 
 /*
+ * LayerNorm of the pair representation fused with the bias-free linear
+ * projection that produces the queries, keys, values, gate and pair bias of
+ * triangle attention (MegaFold technical summary, "Methodik" section 3
+ * "EvoFusion", Umfang and Mechanismus: the normalised N x N x C tensor is not
+ * written to HBM between normalisation and projection).  For every row
+ * r = (b, i, j):
+ *
+ *   y[r, c]   = (z[r, c] - mean_c z[r, :]) / sqrt(var_c z[r, :] + eps)
+ *               * gamma[c] + beta[c]      (var: mean squared deviation)
+ *   out[r, o] = sum_c y[r, c] w[o, c]     (y rounded to bf16, fp32 sums)
+ *   q[b, i, j, h, d] = out[r, h*D + d],          k: + H*D,  v: + 2*H*D,
+ *   g[b, i, j, h, d] = out[r, 3*H*D + h*D + d],  pair_bias[b, h, i, j] = out[r, 4*H*D + h]
+ *
+ *  z          : [B, N, N, C] device bf16, dense (C contiguous), 16-byte aligned.
+ *  gamma, beta: [C] device fp32.
+ *  w          : [4*H*D + H, C] device bf16, dense row-major, 16-byte aligned.
+ *  eps        : > 0, added to the variance.
+ *  q, k, v, g : [B, N, N, H, D] device bf16, dense, 16-byte aligned, written
+ *               (the pair projections in the layout the attention reads as
+ *               starting- or ending-node views).
+ *  pair_bias  : [B, H, N, N] device bf16, dense, written.
+ * Supported: C = 128, H * D = 128, H <= 8, B * N * N < 2^31 (otherwise
+ * EVOATTN_ERR_UNSUPPORTED).  g is the gate's pre-activation: the attention
+ * applies the sigmoid.  Returns EVOATTN_OK once the kernel is enqueued.
+ */
+evoattn_status evoattn_ln_proj(const void* z, const float* gamma, const float* beta,
+                               const void* w, float eps,
+                               void* q, void* k, void* v, void* g, void* pair_bias,
+                               int B, int N, int C, int H, int D, cudaStream_t stream);
+
+/*
  * Testing hook for the bounded-wait failure path; not needed in normal use.
  * Applies to every tcgen05 kernel enqueued after the call, on any device, by
  * any thread of the process.

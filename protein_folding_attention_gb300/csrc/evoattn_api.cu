@@ -136,6 +136,31 @@ const char* evoattn_status_string(evoattn_status s) {
   return "unknown status";
 }
 
+evoattn_status evoattn_ln_proj(const void* z, const float* gamma, const float* beta,
+                               const void* w, float eps, void* q, void* k, void* v, void* g,
+                               void* pair_bias, int B, int N, int C, int H, int D,
+                               cudaStream_t stream) {
+  if (!z || !gamma || !beta || !w || !q || !k || !v || !g || !pair_bias)
+    return EVOATTN_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || C < 1 || H < 1 || D < 1) return EVOATTN_ERR_INVALID_ARG;
+  if (!(eps > 0.f) || !(eps < INFINITY)) return EVOATTN_ERR_INVALID_ARG;
+  if (C != 128 || H * D != 128 || H > 8) return EVOATTN_ERR_UNSUPPORTED;
+  if ((uint64_t)B * N * N > 0x7FFFFFFFull) return EVOATTN_ERR_UNSUPPORTED;
+  auto a16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+  if (!a16(z) || !a16(w) || !a16(q) || !a16(k) || !a16(v) || !a16(g) ||
+      reinterpret_cast<uintptr_t>(gamma) % 4 || reinterpret_cast<uintptr_t>(beta) % 4 ||
+      reinterpret_cast<uintptr_t>(pair_bias) % 2)
+    return EVOATTN_ERR_ALIGNMENT;
+  bool ok = false;
+  unsigned int* status = status_word(&ok);
+  if (!ok) return EVOATTN_ERR_CUDA;
+  bool tmap_ok = true;
+  cudaError_t e = bf16_ln_proj(z, gamma, beta, w, eps, q, k, v, g, pair_bias, B, N, H,
+                               wait_base(status), stream, &tmap_ok);
+  if (!tmap_ok) return EVOATTN_ERR_ALIGNMENT;
+  return cuda_status(e);
+}
+
 evoattn_status evoattn_get_device_status(cudaStream_t stream, int* device_status) {
   if (!device_status) return EVOATTN_ERR_INVALID_ARG;
   bool ok = false;

@@ -34,6 +34,11 @@ inline WaitCfg launch_wait(const WaitCfg& base) {
 cudaError_t bf16_fwd(const Problem& P, const Bf16Ptrs& a, const WaitCfg& wait,
                      cudaStream_t st, bool* tmap_ok);
 
+// LayerNorm + projection (EvoFusion upstream); C = 128 and H * D = 128.
+cudaError_t bf16_ln_proj(const void* z, const float* gamma, const float* beta, const void* w,
+                         float eps, void* q, void* k, void* v, void* g, void* bias, int B, int N,
+                         int H, const WaitCfg& wait, cudaStream_t st, bool* tmap_ok);
+
 size_t bf16_bwd_workspace_bytes(const Problem& P, unsigned flags);
 // `events` (nullable): 5 caller-owned events recorded around the stages.
 cudaError_t bf16_bwd(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,

@@ -60,6 +60,9 @@ def load(path: str = LIB_PATH):
     lib.evoattn_status_string.restype = ctypes.c_char_p
     lib.evoattn_version.argtypes = []
     lib.evoattn_version.restype = i
+    lib.evoattn_ln_proj.argtypes = [vp, fp, fp, vp, ctypes.c_float, vp, vp, vp, vp, vp,
+                                    i, i, i, i, i, vp]
+    lib.evoattn_ln_proj.restype = i
     lib.evoattn_debug_set_wait.argtypes = [ctypes.c_ulonglong, i]
     lib.evoattn_debug_set_wait.restype = i
     _lib = lib
@@ -177,6 +180,28 @@ def bwd(q, k, v, pair_bias, mask, gate, out, lse, dout, flags=DBIAS_DETERMINISTI
         st = lib.evoattn_bwd_profiled(*args, handles)
     _check(st, "evoattn_bwd")
     return {"dq": dq, "dk": dk, "dv": dv, "dbias": dbias, "dgate": dgate}
+
+
+def ln_proj(z, gamma, beta, w, H, D, eps=1e-5, out=None, stream=None):
+    """EvoFusion upstream stack: LayerNorm of z [B, N, N, C] (bf16, dense) with
+    gamma, beta [C] (fp32), then the bias-free projection w [4*H*D + H, C]
+    (bf16).  Returns (q, k, v, g, pair_bias): q..g [B, N, N, H, D] bf16 and
+    pair_bias [B, H, N, N] bf16 (see evoattn_ln_proj).  `out` may supply the
+    five output tensors."""
+    lib = load()
+    B, N, N2, C = z.shape
+    if N2 != N:
+        raise ValueError("z must be [B, N, N, C]")
+    if out is None:
+        mk = lambda: torch.empty((B, N, N, H, D), device=z.device, dtype=torch.bfloat16)
+        out = (mk(), mk(), mk(), mk(),
+               torch.empty((B, H, N, N), device=z.device, dtype=torch.bfloat16))
+    q, k, v, g, bias = out
+    st = lib.evoattn_ln_proj(_ptr(z), _ptr(gamma), _ptr(beta), _ptr(w), float(eps),
+                             _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(bias),
+                             B, N, C, H, D, _stream(stream))
+    _check(st, "evoattn_ln_proj")
+    return q, k, v, g, bias
 
 
 def debug_set_wait(limit_ns: int = 0, stall: bool = False) -> None:

@@ -158,3 +158,22 @@ def make_inputs(w: Workload, device="cpu", seed=None):
 def small(name="case", B=1, S=3, N=5, H=2, D=4, **kw) -> Workload:
     """A small workload for tests (default: the finite-difference shape)."""
     return Workload(name, B=B, S=S, N=N, H=H, D=D, **kw)
+
+
+def make_fusion_inputs(B, N, C, H, D, seed=0, device="cpu"):
+    """Seeded inputs of the EvoFusion upstream stack (LayerNorm + projection):
+    z [B, N, N, C] bf16 with a per-channel offset and scale (so the
+    normalisation has a mean and a spread to remove), gamma ~ 1 + 0.1 N(0,1)
+    and beta ~ 0.1 N(0,1) in fp32, and w [4*H*D + H, C] bf16 ~ N(0, 1/C) (so
+    every projected value is of order one).  Draw order: channel offsets,
+    channel scales, z, gamma, beta, w."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    f32 = dict(device=device, dtype=torch.float32)
+    mu = torch.randn(C, generator=gen, **f32)
+    sd = torch.rand(C, generator=gen, **f32) * 1.5 + 0.5
+    z = (torch.randn(B, N, N, C, generator=gen, **f32) * sd + mu).to(torch.bfloat16)
+    gamma = 1.0 + 0.1 * torch.randn(C, generator=gen, **f32)
+    beta = 0.1 * torch.randn(C, generator=gen, **f32)
+    w = (torch.randn(4 * H * D + H, C, generator=gen, **f32) * C ** -0.5).to(torch.bfloat16)
+    return {"z": z, "gamma": gamma, "beta": beta, "w": w}

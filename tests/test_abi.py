@@ -163,3 +163,22 @@ def torch_bf16():
 def torch_f32():
     import torch
     return torch.float32
+
+
+def call_ln_proj(lib, *, z=FAKE, w=FAKE, q=FAKE, eps=1e-5, B=1, N=8, C=128, H=4, D=32):
+    return lib.evoattn_ln_proj(z, FAKE, FAKE, w, eps, q, FAKE, FAKE, FAKE, FAKE,
+                               B, N, C, H, D, None)
+
+
+def test_ln_proj_rejects_bad_arguments(lib):
+    assert call_ln_proj(lib, z=None) == evoattn.ERR_INVALID_ARG
+    assert call_ln_proj(lib, q=None) == evoattn.ERR_INVALID_ARG
+    assert call_ln_proj(lib, N=0) == evoattn.ERR_INVALID_ARG
+    assert call_ln_proj(lib, eps=0.0) == evoattn.ERR_INVALID_ARG
+    assert call_ln_proj(lib, eps=float("nan")) == evoattn.ERR_INVALID_ARG
+    assert call_ln_proj(lib, C=64) == evoattn.ERR_UNSUPPORTED
+    assert call_ln_proj(lib, H=4, D=16) == evoattn.ERR_UNSUPPORTED   # H*D != 128
+    assert call_ln_proj(lib, H=16, D=8) == evoattn.ERR_UNSUPPORTED   # more than 8 heads
+    assert call_ln_proj(lib, B=1, N=50000) == evoattn.ERR_UNSUPPORTED  # B*N*N >= 2^31
+    assert call_ln_proj(lib, z=ctypes.c_void_p((1 << 20) + 8)) == evoattn.ERR_ALIGNMENT
+    assert call_ln_proj(lib, w=ctypes.c_void_p((1 << 20) + 2)) == evoattn.ERR_ALIGNMENT

@@ -64,3 +64,18 @@ def test_reference_arm_json_line():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_memory_fit_recovers_a_linear_footprint():
+    """The fit of held device bytes against L = B*S*H*N*D and B*H*N^2 returns
+    the coefficients of an exactly linear footprint and a zero residual; a
+    cubic term shows up as a large residual."""
+    pts = []
+    for L, n2 in ((100, 10), (800, 40), (6400, 160), (3000, 90)):
+        pts.append({"L": L, "BHN2": n2, "device_bytes": 26 * L + 6 * n2 + 1000})
+    f = bench.memory_fit(pts)
+    assert f["bytes_per_L"] == pytest.approx(26.0)
+    assert f["bytes_per_BHN2"] == pytest.approx(6.0)
+    assert f["max_rel_residual"] < 1e-9
+    cubic = [dict(p, device_bytes=p["device_bytes"] + p["L"] ** 1.5) for p in pts]
+    assert bench.memory_fit(cubic)["max_rel_residual"] > 1e-2

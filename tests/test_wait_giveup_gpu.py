@@ -74,3 +74,20 @@ def test_default_limit_is_restored():
     for _ in range(3):
         evoattn.fwd(*args)
     assert evoattn.device_status() == evoattn.OK
+
+
+def test_ln_proj_gives_up_and_recovers():
+    """The fused LayerNorm + projection kernel: its LayerNorm warps' first
+    wait stalls, every CTA gives up, the status reads ERR_TIMEOUT, and the
+    next call matches the oracle."""
+    from oracle import fusion
+    from helpers import rel_l2
+    x = synthetic.make_fusion_inputs(1, 40, 128, 4, 32, seed=8)
+    xd = {k: v.to("cuda") for k, v in x.items()}
+    run = lambda: evoattn.ln_proj(xd["z"], xd["gamma"], xd["beta"], xd["w"], 4, 32)
+    assert _stalled(run) == evoattn.ERR_TIMEOUT
+    out = run()
+    assert evoattn.device_status() == evoattn.OK
+    ref = fusion.ln_proj(x["z"], x["gamma"], x["beta"], x["w"], 4, 32)
+    for got, r in zip(out, ref):
+        assert rel_l2(got, r) <= 5e-3
