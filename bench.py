@@ -192,6 +192,39 @@ def measure_config(w, dev, peak, steps=5, warmup=3):
     return res
 
 
+def measure_ln_proj(N, dev, peaks, steps=10, warmup=3, B=1, C=128, H=4, D=32):
+    """The EvoFusion upstream stack (LayerNorm + q/k/v/g/pair-bias projection)
+    on the [B, N, N, C] pair representation: CUDA-event time, algorithmic HBM
+    bytes (z read, weights read, five outputs written) against the measured
+    copy bandwidth, and the projection's TFLOP/s."""
+    import torch
+
+    from protein_folding_attention_gb300 import evoattn, synthetic
+    x = synthetic.make_fusion_inputs(B, N, C, H, D, seed=N, device=dev)
+    out = evoattn.ln_proj(x["z"], x["gamma"], x["beta"], x["w"], H, D)
+    for _ in range(warmup):
+        evoattn.ln_proj(x["z"], x["gamma"], x["beta"], x["w"], H, D, out=out)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        a.record()
+        evoattn.ln_proj(x["z"], x["gamma"], x["beta"], x["w"], H, D, out=out)
+        b.record()
+    torch.cuda.synchronize(dev)
+    if evoattn.device_status() != evoattn.OK:
+        raise RuntimeError("device status set by evoattn_ln_proj")
+    t = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e-3
+    rows = B * N * N
+    nout = 4 * H * D + H
+    bytes_ = rows * C * 2 + nout * C * 2 + rows * nout * 2
+    flops = 2 * rows * C * nout
+    gbs = bytes_ / t / 1e9
+    return {"workload": f"pair_ln_proj_n{N}", "B": B, "N": N, "C": C, "H": H, "D": D,
+            "ms": t * 1e3, "hbm_bytes": bytes_, "hbm_gbs": gbs,
+            "frac_of_hbm_peak": gbs / peaks["hbm_gbs"], "tflops": flops / t / 1e12,
+            "normalised_tensor_bytes_not_written": rows * C * 2}
+
+
 def memory_fit(points):
     """Least-squares fit of device bytes = a*L + b*BHN2 + c over the given
     {"L", "BHN2", "device_bytes"} points (L = B*S*H*N*D, BHN2 = B*H*N*N).
@@ -510,6 +543,9 @@ def run_ours(args, w):
         for name in PER_CONFIG:
             per_config[name] = measure_config(synthetic.WORKLOADS[name], dev, peak)
         per_config["memory_fit"] = memory_fit([per_config[n] for n in PER_CONFIG])
+    evofusion = None
+    if rank == 0 and not args.no_per_config:
+        evofusion = {f"n{n}": measure_ln_proj(n, dev, peaks) for n in (384, 768)}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
@@ -535,7 +571,7 @@ def run_ours(args, w):
             "memory": memory,
             "dbias_variants": dbias_variants,
             "roofline": roof, "sfu": sfu, "cpu_baseline": cpu, "e2e": e2e,
-            "per_config": per_config,
+            "per_config": per_config, "evofusion": evofusion,
             "clocks": clocks.summary(),
             "gpu_launches": args.steps * 6,
         }

@@ -26,7 +26,11 @@
 //                (bf16, in the swizzled layout the MMA reads) and computes its
 //                H pair-bias outputs with fp32 FMAs
 //   warps 8-11   epilogue warpgroup: thread = TMEM lane = row; tensor memory ->
-//                bf16 -> q, k, v, g rows (256 contiguous bytes each)
+//                bf16 -> a 4 KB staging buffer per warp (32 rows x 128 B, in
+//                the 128-byte swizzle) -> one TMA tensor store per chunk.  (A
+//                thread storing its own row would touch 32 rows per store
+//                instruction and saturate the load/store unit that the
+//                LayerNorm warps share.)
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -57,7 +61,8 @@ struct FusionCfg {
   static constexpr uint32_t OFF_Z = OFF_W + 2 * WHALF;       // NZ x [2 halves][128 rows][128 B]
   static constexpr uint32_t OFF_WB = OFF_Z + NZ * ZTILE;     // [HMAX][C] fp32
   static constexpr uint32_t OFF_GB = OFF_WB + HMAX * C * 4;  // gamma[C], beta[C] fp32
-  static constexpr uint32_t SMEM = OFF_GB + 2 * C * 4;
+  static constexpr uint32_t OFF_STAGE = OFF_GB + 2 * C * 4;  // 4 warps x 32 rows x 128 B
+  static constexpr uint32_t SMEM = OFF_STAGE + 4 * 32 * 128;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
   static constexpr int THREADS = 384;
   static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_LN = 232, REGS_EPI = 216;
@@ -77,15 +82,38 @@ struct FusionParams {
   WaitCfg wc;
 };
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int c0,
+                                             int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(c0), "r"(c1), "r"(smem_u32(src))
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The staging buffer may be rewritten once the bulk stores committed so far
+// have read it.
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Every bulk store committed so far has completed.
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(384, 1)
     evoattn_ln_proj_kernel(const __grid_constant__ CUtensorMap tm_z,
-                           const __grid_constant__ CUtensorMap tm_w, const FusionParams p) {
+                           const __grid_constant__ CUtensorMap tm_w,
+                           const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ CUtensorMap tm_g, const FusionParams p) {
   using C = FusionCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_w, bar_z_full[C::NZ], bar_z_empty[C::NZ], bar_y_ready[C::NZ],
-      bar_mma_done, bar_tmem_free, bar_drain, bar_never;
+      bar_mma_done[2], bar_tmem_free[2], bar_drain, bar_never;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -100,8 +128,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bar_z_empty[i], 1);     // the tile's MMAs have read it
       mbar_init(&bar_y_ready[i], 128);   // every row normalised
     }
-    mbar_init(&bar_mma_done, 1);
-    mbar_init(&bar_tmem_free, 128);      // the epilogue has read the tile's outputs
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_mma_done[i], 1);
+      mbar_init(&bar_tmem_free[i], 128);  // the epilogue has read the half's outputs
+    }
     mbar_init(&bar_drain, 1);
     mbar_init(&bar_never, 1);            // nothing arrives: the stall test waits on it
     fence_barrier_init();
@@ -185,14 +215,18 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_w, 0, wctx));
       for (int n = 0; n < n_my && ok; ++n) {
         const int st = n % C::NZ;
-        ok = mbar_wait(&bar_y_ready[st], (n / C::NZ) & 1, wctx);
-        if (ok && n > 0) ok = mbar_wait(&bar_tmem_free, (n - 1) & 1, wctx);
-        ok = __all_sync(0xffffffffu, ok);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_y_ready[st], (n / C::NZ) & 1, wctx));
         if (!ok) break;
-        tc_fence_after();
         const uint64_t da = da0 + ((uint32_t)(st * C::ZTILE) >> 4);
+        // half nh (q, k or v, g) once the epilogue has read the previous
+        // tile's outputs of that half
 #pragma unroll
-        for (int nh = 0; nh < 2; ++nh)
+        for (int nh = 0; nh < 2; ++nh) {
+          if (n > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar_tmem_free[nh], (n - 1) & 1, wctx));
+            if (!ok) break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t a = da + ((uint32_t)((kk >> 2) * C::HALF + (kk & 3) * 32) >> 4);
@@ -200,11 +234,13 @@ __global__ void __launch_bounds__(384, 1)
                 db0 + ((uint32_t)((kk >> 2) * C::WHALF + nh * 256 * 128 + (kk & 3) * 32) >> 4);
             if (elect_one()) umma_ss(tmem + 256 * nh, a, b, id, kk > 0 ? 1u : 0u);
           }
-        if (elect_one()) {
-          umma_commit(&bar_z_empty[st]);
-          umma_commit(&bar_mma_done);
+          if (elect_one()) {
+            if (nh == 1) umma_commit(&bar_z_empty[st]);
+            umma_commit(&bar_mma_done[nh]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
+        if (!ok) break;
       }
       if (elect_one()) umma_commit(&bar_drain);
       __syncwarp();
@@ -307,40 +343,59 @@ __global__ void __launch_bounds__(384, 1)
     const int quad = warp & 3;
     const int m = quad * 32 + lane;  // TMEM lane = row within the tile
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-    __nv_bfloat16* outs[4] = {p.q, p.k, p.v, p.g};
+    const CUtensorMap* outs[4] = {&tm_q, &tm_k, &tm_v, &tm_g};
     bool ok = true;
     for (int n = 0; n < n_my && ok; ++n) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done, n & 1, wctx));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done[0], n & 1, wctx));
       if (!ok) break;
       tc_fence_after();
-      const int64_t row = (int64_t)((int)blockIdx.x + n * (int)gridDim.x) * C::BM + m;
-      const bool live = row < p.rows;
-      // output o of the row: columns 128 o .. 128 o + 127, 32 at a time, each
-      // 32-column chunk stored as 64 contiguous bytes
+      const int row0 = ((int)blockIdx.x + n * (int)gridDim.x) * C::BM + quad * 32;
+      // this warp's staging buffer: row r, 16-byte chunk c at chunk c ^ (r % 8)
+      uint8_t* stg = smem + C::OFF_STAGE + quad * 4096;
+      // each output: 128 columns in two chunks of 64 (128 bytes of a row)
+#pragma unroll 1
+      for (int o = 0; o < 4 && ok; ++o) {
+        if (o == 2) {  // v and g: the second half of tensor memory
+          ok = __all_sync(0xffffffffu, mbar_wait(&bar_mma_done[1], n & 1, wctx));
+          if (!ok) break;
+          tc_fence_after();
+        }
 #pragma unroll
-      for (int o = 0; o < 4; ++o) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + 128 * o + 32 * c, r);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(lane_base + 128 * o + 64 * hh, ra);
+          tmem_ld32(lane_base + 128 * o + 64 * hh + 32, rb);
+          // the previous chunk's bulk store has read the staging buffer
+          if (lane == 0) tma_store_wait_read();
+          __syncwarp();
           tmem_wait_ld();
-          reg_fence32(r);
-          uint32_t pk[16];
+          reg_fence32(ra);
+          reg_fence32(rb);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(outs[o] + row * C::HD + 32 * c);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t* src = c < 4 ? &ra[8 * c] : &rb[8 * (c - 4)];
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(pack_bf16(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                           pack_bf16(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                           pack_bf16(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                           pack_bf16(__uint_as_float(src[6]), __uint_as_float(src[7])));
           }
+          // generic writes, read by the bulk copy (rows beyond the tensor are
+          // dropped by the copy)
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tma_store_2d(outs[o], stg, 64 * hh, row0);
+          __syncwarp();
+        }
+        if (o == 1 || o == 3) {  // a half of tensor memory is read
+          tc_fence_before();
+          mbar_arrive(&bar_tmem_free[o >> 1]);
         }
       }
-      // the tile's outputs are read: the next tile's MMAs may start
-      tc_fence_before();
-      mbar_arrive(&bar_tmem_free);
+      if (!ok) break;
     }
+    if (lane == 0) tma_store_wait_all();
+    __syncwarp();
     teardown();
   }
 }
@@ -352,13 +407,21 @@ cudaError_t bf16_ln_proj(const void* z, const float* gamma, const float* beta, c
                          int H, const WaitCfg& wait, cudaStream_t st, bool* tmap_ok) {
   using C = FusionCfg;
   const uint64_t rows = (uint64_t)B * N * N;
-  CUtensorMap tz, tw;
+  CUtensorMap tz, tw, tq, tk, tv, tg;
   const uint64_t zdims[2] = {(uint64_t)C::C, rows};
   const uint64_t zstr[1] = {(uint64_t)C::C * 2};
   const uint32_t box[2] = {64, 128};
   const uint64_t wdims[2] = {(uint64_t)C::C, (uint64_t)C::NOUT};
+  // outputs [rows, HD]: one bulk store writes 32 rows x 64 columns
+  const uint64_t odims[2] = {(uint64_t)C::HD, rows};
+  const uint64_t ostr[1] = {(uint64_t)C::HD * 2};
+  const uint32_t obox[2] = {64, 32};
   if (!make_tmap_bf16(&tz, z, 2, zdims, zstr, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_bf16(&tw, w, 2, wdims, zstr, box, CU_TENSOR_MAP_SWIZZLE_128B)) {
+      !make_tmap_bf16(&tw, w, 2, wdims, zstr, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16(&tq, q, 2, odims, ostr, obox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16(&tk, k, 2, odims, ostr, obox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16(&tv, v, 2, odims, ostr, obox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16(&tg, g, 2, odims, ostr, obox, CU_TENSOR_MAP_SWIZZLE_128B)) {
     *tmap_ok = false;
     return cudaErrorInvalidValue;
   }
@@ -393,7 +456,7 @@ cudaError_t bf16_ln_proj(const void* z, const float* gamma, const float* beta, c
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)std::min<uint64_t>(tiles, (uint64_t)std::max(sms, 1));
-  kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tz, tw, fp);
+  kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tz, tw, tq, tk, tv, tg, fp);
   return cudaGetLastError();
 }
 
