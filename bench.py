@@ -30,9 +30,11 @@ sys.path.insert(0, ROOT)
 METRIC = "EvoAttention fwd+bwd TFLOP/s and % of GB300 BF16 dense peak (N=768 triangle attn)"
 WORKLOAD = "pairformer_end_n768"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# ex2.approx.f32 results per clock per SM, microbenchmarked on GB300 (8 per
-# sub-partition); the third roofline of the path, beside HBM and tensor cores
-EX2_PER_CLK_PER_SM = 32
+# ex2.approx.f32 results per clock per SM on GB300: the XU pipe takes a warp
+# instruction every 2 clocks per sub-partition (16 per sub-partition); a
+# register-only run of the softmax inner loop reached 55.6 per clock per SM.
+# The third roofline of the path, beside HBM and tensor cores.
+EX2_PER_CLK_PER_SM = 64
 
 
 def load_peaks():
