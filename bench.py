@@ -224,6 +224,7 @@ def measure_ln_proj(N, dev, peaks, steps=10, warmup=3, B=1, C=128, H=4, D=32):
     return {"workload": f"pair_ln_proj_n{N}", "B": B, "N": N, "C": C, "H": H, "D": D,
             "ms": t * 1e3, "hbm_bytes": bytes_, "hbm_gbs": gbs,
             "frac_of_hbm_peak": gbs / peaks["hbm_gbs"], "tflops": flops / t / 1e12,
+            "traffic": profiled_traffic("evoattn_ln_proj_kernel", f"pair_ln_proj_n{N}"),
             "normalised_tensor_bytes_not_written": rows * C * 2}
 
 
@@ -322,10 +323,11 @@ def run_ours(args, w):
     def fwd():
         evoattn.fwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out=out, lse=lse)
 
-    def bwd(events=None, flags=evoattn.DBIAS_DETERMINISTIC):
+    def bwd(events=None, flags=evoattn.DBIAS_DETERMINISTIC, workspace=None):
         evoattn.bwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out, lse,
                     x["dout"], flags=flags, dq=grads["dq"], dk=grads["dk"], dv=grads["dv"],
-                    dbias=dbias, dgate=grads["dgate"], workspace=wsp, stage_events=events)
+                    dbias=dbias, dgate=grads["dgate"],
+                    workspace=wsp if workspace is None else workspace, stage_events=events)
 
     def barrier():
         if pg is not None:
@@ -405,6 +407,32 @@ def run_ours(args, w):
         "atomic": {"dbias_ms": stage_a[2] * 1e3, "reduce_ms": stage_a[3] * 1e3,
                    "bwd_ms": sum(stage_a) * 1e3},
     }
+
+    # ---- dQ: the deterministic mode (per-key-tile slices, ordered sum) timed
+    # beside the default atomic accumulation; its larger workspace is
+    # allocated here, outside the measured steps
+    wsp_det = torch.empty(evoattn.workspace_size(B, S, H, N, D, w.torch_dtype,
+                                                 flags=evoattn.DQ_DETERMINISTIC),
+                          device=dev, dtype=torch.uint8)
+    ev_d = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+            for _ in range(max(3, args.steps // 2))]
+    for _ in range(2):
+        bwd(None, evoattn.DQ_DETERMINISTIC, wsp_det)
+    for e in ev_d:
+        bwd(e, evoattn.DQ_DETERMINISTIC, wsp_det)
+    barrier()
+    stage_d = [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev_d) * 1e-3
+               for k in range(n_ev - 1)]
+    dq_modes = {
+        "atomic": {"dkdv_ms": stage[1] * 1e3, "reduce_ms": stage[3] * 1e3,
+                   "bwd_ms": sum(stage) * 1e3, "workspace_bytes": int(wsp.numel())},
+        "deterministic": {"dkdv_ms": stage_d[1] * 1e3, "reduce_ms": stage_d[3] * 1e3,
+                          "bwd_ms": sum(stage_d) * 1e3,
+                          "workspace_bytes": int(wsp_det.numel())},
+    }
+    del wsp_det
+    if evoattn.device_status() != evoattn.OK:
+        raise RuntimeError("device status after the dQ-mode timing")
 
     # ---- exponential unit: the forward, dK/dV and dbias kernels each
     # evaluate exactly one ex2 per logit; peak = EX2_PER_CLK_PER_SM x SMs x
@@ -572,6 +600,7 @@ def run_ours(args, w):
             "frac_of_peak": value / ws / peak,
             "memory": memory,
             "dbias_variants": dbias_variants,
+            "dq_modes": dq_modes,
             "roofline": roof, "sfu": sfu, "cpu_baseline": cpu, "e2e": e2e,
             "per_config": per_config, "evofusion": evofusion,
             "clocks": clocks.summary(),
@@ -614,7 +643,17 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--evofusion-only", type=int, default=0, metavar="N",
+                    help="profiling only: time the LayerNorm + projection kernel on the "
+                         "[1, N, N, 128] pair representation and print its JSON")
     args = ap.parse_args()
+    if args.evofusion_only:
+        import torch
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        peaks, _ = load_peaks()
+        print(json.dumps(measure_ln_proj(args.evofusion_only, dev, peaks)))
+        return 0
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
     from protein_folding_attention_gb300 import synthetic

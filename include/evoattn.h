@@ -96,6 +96,7 @@ typedef enum { EVOATTN_BF16 = 0, EVOATTN_F32 = 1 } evoattn_dtype;
 /* evoattn_bwd flags */
 #define EVOATTN_DBIAS_DETERMINISTIC 0u  /* fixed s-slots + ordered sum: bit-identical */
 #define EVOATTN_DBIAS_ATOMIC 1u         /* s-slot partials added with fp32 atomics */
+#define EVOATTN_DQ_DETERMINISTIC 2u     /* per-key-tile dQ slices + ordered sum */
 
 /*
  * Forward (MegaFold technical summary, "Methodik" section 1 "EvoFlash-3D",
@@ -123,8 +124,11 @@ evoattn_status evoattn_fwd(const void* q, const int64_t q_strides[5],
 
 /*
  * Bytes of device workspace evoattn_bwd needs for this problem (0 on invalid
- * sizes).  Linear in B*S*H*N*D plus O(B*H*N*N) for the dbias partial sums;
- * never proportional to B*S*H*N*N.
+ * sizes or flags).  Linear in B*S*H*N*D plus O(B*H*N*N) for the dbias
+ * partial sums; never proportional to B*S*H*N*N -- except with
+ * EVOATTN_DQ_DETERMINISTIC on the BF16 path, which adds ceil(N/128) - 1
+ * further fp32 copies of dq (4 * B*S*H*N*D bytes each): the price of a fixed
+ * summation order without giving up the load balance of the dK/dV kernel.
  */
 size_t evoattn_bwd_workspace_size(int B, int S, int H, int N, int D,
                                   evoattn_dtype dtype, unsigned flags);
@@ -144,7 +148,19 @@ size_t evoattn_bwd_workspace_size(int B, int S, int H, int N, int D,
  *  flags                    : EVOATTN_DBIAS_DETERMINISTIC (bit-identical
  *                             dbias from run to run and box to box) or
  *                             EVOATTN_DBIAS_ATOMIC (same partials combined
- *                             with atomics; order-dependent rounding).
+ *                             with atomics; order-dependent rounding), OR-ed
+ *                             with EVOATTN_DQ_DETERMINISTIC to make dq
+ *                             bit-identical too: by default the BF16 path
+ *                             adds the dQ partial of every key tile into an
+ *                             fp32 buffer with atomics (rounding depends on
+ *                             their order); with the flag each key tile
+ *                             stores its partial into a slice of its own
+ *                             and the slices are summed in key-tile order
+ *                             (workspace: ceil(N/128) fp32 copies of dq
+ *                             instead of one).  dk, dv and dgate are
+ *                             bit-identical in every mode; the F32 path is
+ *                             deterministic whatever the flags.  Other bits
+ *                             set: EVOATTN_ERR_INVALID_ARG.
  *  workspace                : device, 256-byte aligned, at least
  *                             evoattn_bwd_workspace_size(...) bytes; the
  *                             library overwrites it; it must not be used by

@@ -15,11 +15,13 @@
 //   k_pre    delta, dgate and dOa (bf16) per row; zeroes the fp32 dQ buffer
 //   k_dkdv   CTA = (b, s, h, key tile): loops over query tiles with dK, dV
 //            accumulating in tensor memory; dQ partial sums are added into
-//            the fp32 buffer with vector atomics
+//            the fp32 buffer with vector atomics (deterministic dQ: each key
+//            tile stores its partial into a slice of its own instead)
 //   k_dbias  CTA = (b, h, query tile, key tile, s-slot): loops over the s of
 //            its slot, recomputing S and dP, accumulating dS in tensor memory;
 //            writes one partial per slot (or adds it atomically)
-//   k_reduce ordered sum of the slot partials -> dbias; fp32 dQ -> bf16 dq
+//   k_reduce ordered sum of the slot partials -> dbias; fp32 dQ (the slices
+//            summed in key-tile order) -> bf16 dq
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -64,7 +66,8 @@ inline int dbias_slots(const Problem& P) {
 struct Workspace {
   __nv_bfloat16* dOa;  // [B,S,H,N,D], dense in the memory order of out
   float* delta;        // [B,S,H,N]
-  float* dq_acc;       // [B,S,H,N,D] dense fp32
+  float* dq_acc;       // [dq_slices, B,S,H,N,D] dense fp32
+  int dq_slices;       // 1 (atomic sums) or one per key tile (deterministic dQ)
   float* partial;      // [slots, B, H, N, N] fp32 (deterministic mode)
   size_t bytes;
 };
@@ -76,7 +79,9 @@ Workspace carve(const Problem& P, unsigned flags, void* base) {
   uint8_t* b = static_cast<uint8_t*>(base);
   w.dOa = reinterpret_cast<__nv_bfloat16*>(b + off); off = align256(off + L * 2);
   w.delta = reinterpret_cast<float*>(b + off); off = align256(off + (size_t)P.rows() * 4);
-  w.dq_acc = reinterpret_cast<float*>(b + off); off = align256(off + L * 4);
+  w.dq_slices = (flags & EVOATTN_DQ_DETERMINISTIC) ? (P.N + 127) / 128 : 1;
+  w.dq_acc = reinterpret_cast<float*>(b + off);
+  off = align256(off + (size_t)w.dq_slices * L * 4);
   w.partial = reinterpret_cast<float*>(b + off);
   if (!(flags & EVOATTN_DBIAS_ATOMIC))
     off = align256(off + (size_t)dbias_slots(P) * P.B * P.H * P.N * P.N * 4);
@@ -199,10 +204,12 @@ __global__ void __launch_bounds__(256) k_pre(const PreParams p) {
       }
       *reinterpret_cast<uint4*>(p.dOa + p.a.at(b, s, h, j, 8 * part)) = pack8(a);
       // the fp32 dQ buffer (dense) is zeroed in unit order: 32 contiguous
-      // bytes per unit
-      float4* z = reinterpret_cast<float4*>(p.dq_acc + 8 * u);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      // bytes per unit (not needed when every key tile stores its own slice)
+      if (p.dq_acc) {
+        float4* z = reinterpret_cast<float4*>(p.dq_acc + 8 * u);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, off);
@@ -290,6 +297,10 @@ struct DkdvParams {
   const float* lse;
   const float* delta;
   float* dq_acc;
+  // deterministic dQ: key tile kt stores its partial, plain, into slice kt
+  // (slice stride dq_slice elements) instead of adding it atomically
+  int dq_det;
+  int64_t dq_slice;
   __nv_bfloat16 *dk, *dv;
   Strides5 sdk, sdv;
   WaitCfg wc;
@@ -623,9 +634,10 @@ __global__ void __launch_bounds__(384, 1)
     const float inv_sqrt_d = rsqrtf((float)D);
     const float2 c1c1 = make_float2(c1, c1), l2l2 = make_float2(kLog2e, kLog2e),
                  isd = make_float2(inv_sqrt_d, inv_sqrt_d);
-    // dQ partial of tile t (query tile jt_t of the item at row0_t): lane =
-    // query; this warpgroup adds half of D
-    auto dq_epilogue = [&](int t, int64_t row0_t, int jt_t) {
+    // dQ partial of tile t (query tile jt_t of the item at row0_t, key tile
+    // kt_t): lane = query; this warpgroup adds (or, deterministic, stores)
+    // half of D
+    auto dq_epilogue = [&](int t, int64_t row0_t, int jt_t, int kt_t) {
       uint32_t q16[D / 2];
       if constexpr (D == 32) {
         tmem_ld16(lane_base + C::T_DQ + (t & 1) * D + 16 * wg,
@@ -642,10 +654,18 @@ __global__ void __launch_bounds__(384, 1)
       const int jg = jt_t * 128 + kl;  // this lane's query row
       if (jg < p.N) {
         float* dst = p.dq_acc + (row0_t + jg) * D + (D / 2) * wg;
+        if (p.dq_det) {
+          float4* d4 = reinterpret_cast<float4*>(dst + kt_t * p.dq_slice);
 #pragma unroll
-        for (int e = 0; e < D / 2; e += 4)
-          red_add_v4(dst + e, __uint_as_float(q16[e]), __uint_as_float(q16[e + 1]),
-                     __uint_as_float(q16[e + 2]), __uint_as_float(q16[e + 3]));
+          for (int e = 0; e < D / 2; e += 4)
+            d4[e / 4] = make_float4(__uint_as_float(q16[e]), __uint_as_float(q16[e + 1]),
+                                    __uint_as_float(q16[e + 2]), __uint_as_float(q16[e + 3]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < D / 2; e += 4)
+            red_add_v4(dst + e, __uint_as_float(q16[e]), __uint_as_float(q16[e + 1]),
+                       __uint_as_float(q16[e + 2]), __uint_as_float(q16[e + 3]));
+        }
       }
     };
     // mask byte of this thread's key in item n, loaded one item ahead so its
@@ -662,7 +682,7 @@ __global__ void __launch_bounds__(384, 1)
     // first tile, by which time the item's last MMAs have completed, so the
     // compute threads never idle on them at an item boundary.
     auto item_end = [&](const DkdvItem& e, int g_last) {
-      dq_epilogue(g_last, e.row0, njt - 1);
+      dq_epilogue(g_last, e.row0, njt - 1, e.kt);
       uint32_t r[D];
       const uint32_t col = wg == 0 ? C::T_DK : C::T_DV;
 #pragma unroll
@@ -765,7 +785,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bar_p_ready);
-        if (jt > 0) dq_epilogue(g - 1, it.row0, jt - 1);  // its MMAs completed (waited above)
+        if (jt > 0) dq_epilogue(g - 1, it.row0, jt - 1, it.kt);  // its MMAs completed (waited above)
       }
       prev = it;
       pending = true;
@@ -1146,7 +1166,8 @@ __global__ void __launch_bounds__(DbiasCfg<D>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
-// k_reduce: dbias = ordered sum of the slot partials; dq = bf16(dq_acc)
+// k_reduce: dbias = ordered sum of the slot partials; dq = bf16 of the dQ
+// slices summed in key-tile order (one slice unless dQ is deterministic)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_dbias_sum(const float* __restrict__ partial,
                                                    float* __restrict__ dbias, int64_t n,
@@ -1170,10 +1191,13 @@ __global__ void __launch_bounds__(256) k_dbias_sum(const float* __restrict__ par
   }
 }
 
-template <int D>
+// SLICED: deterministic dQ, `slices` key-tile partials summed in order; the
+// plain conversion stays a separate instantiation so that its register
+// count (and occupancy) does not pay for the loop
+template <int D, bool SLICED>
 __global__ void __launch_bounds__(256) k_dq_convert(const float* __restrict__ dq_acc,
                                                     __nv_bfloat16* __restrict__ dq, Strides5 sdq,
-                                                    int B, int S, int H, int N) {
+                                                    int B, int S, int H, int N, int slices) {
   constexpr int TPR = D / 8;
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t row = t / TPR;
@@ -1184,7 +1208,15 @@ __global__ void __launch_bounds__(256) k_dq_convert(const float* __restrict__ dq
   const int s = (int)((row / ((int64_t)N * H)) % S);
   const int b = (int)(row / ((int64_t)N * H * S));
   const float4* src = reinterpret_cast<const float4*>(dq_acc + row * D + 8 * part);
-  const float4 a = src[0], c = src[1];
+  float4 a = src[0], c = src[1];
+  if (SLICED) {
+    const int64_t slice4 = (int64_t)B * S * H * N * (D / 4);
+    for (int k = 1; k < slices; ++k) {
+      const float4 x = src[k * slice4], y = src[k * slice4 + 1];
+      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+      c.x += y.x; c.y += y.y; c.z += y.z; c.w += y.w;
+    }
+  }
   const float f[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
   *reinterpret_cast<uint4*>(dq + sdq.at(b, s, h, j, 8 * part)) = pack8(f);
 }
@@ -1246,7 +1278,8 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     pp.gate = static_cast<const __nv_bfloat16*>(a.gate);
     pp.o = P.o; pp.dO = P.dout; pp.g = P.g; pp.dg = P.dg;
     pp.dgate = static_cast<__nv_bfloat16*>(a.dgate);
-    pp.dOa = w.dOa; pp.delta = w.delta; pp.dq_acc = w.dq_acc;
+    pp.dOa = w.dOa; pp.delta = w.delta;
+    pp.dq_acc = w.dq_slices == 1 ? w.dq_acc : nullptr;  // slices are stored, not added to
     constexpr int U = 2;
     const int64_t units = P.rows() * (D / 8);
     k_pre<D, U><<<(unsigned)((units + 256 * U - 1) / (256 * U)), 256, 0, st>>>(pp);
@@ -1266,6 +1299,8 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     dp.n_items = (int)items;
     dp.mask = a.mask; dp.msb = P.mask.b; dp.mss = P.mask.s; dp.msk = P.mask.k;
     dp.lse = a.lse; dp.delta = w.delta; dp.dq_acc = w.dq_acc;
+    dp.dq_det = w.dq_slices > 1 ? 1 : 0;
+    dp.dq_slice = P.rows() * D;
     dp.dk = static_cast<__nv_bfloat16*>(a.dk); dp.dv = static_cast<__nv_bfloat16*>(a.dv);
     dp.sdk = P.dk; dp.sdv = P.dv; dp.wc = launch_wait(wait);
     auto kern = k_dkdv<D, KC>;
@@ -1312,8 +1347,13 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
   }
   {
     const int64_t threads = P.rows() * (D / 8);
-    k_dq_convert<D><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
-        w.dq_acc, static_cast<__nv_bfloat16*>(a.dq), P.dq, P.B, P.S, P.H, P.N);
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    if (w.dq_slices > 1)
+      k_dq_convert<D, true><<<blocks, 256, 0, st>>>(
+          w.dq_acc, static_cast<__nv_bfloat16*>(a.dq), P.dq, P.B, P.S, P.H, P.N, w.dq_slices);
+    else
+      k_dq_convert<D, false><<<blocks, 256, 0, st>>>(
+          w.dq_acc, static_cast<__nv_bfloat16*>(a.dq), P.dq, P.B, P.S, P.H, P.N, 1);
   }
   if (ev) cudaEventRecord(ev[4], st);
   return cudaGetLastError();

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libevoattn.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 BF16, F32 = 0, 1
 DBIAS_DETERMINISTIC, DBIAS_ATOMIC = 0, 1
+DQ_DETERMINISTIC = 2  # OR-ed with either: dq bit-identical too
 
 _lib = None
 _I64_5 = ctypes.c_int64 * 5

@@ -106,7 +106,8 @@ def test_bwd_rejects_bad_arguments(lib):
     assert call_bwd(lib, dq=None) == evoattn.ERR_INVALID_ARG
     assert call_bwd(lib, gate=FAKE, dgate=None) == evoattn.ERR_INVALID_ARG
     assert call_bwd(lib, gate=None, dgate=FAKE) == evoattn.ERR_INVALID_ARG
-    assert call_bwd(lib, flags=2) == evoattn.ERR_INVALID_ARG
+    assert call_bwd(lib, flags=4) == evoattn.ERR_INVALID_ARG
+    assert call_bwd(lib, flags=6) == evoattn.ERR_INVALID_ARG
     assert call_bwd(lib, ws=None) == evoattn.ERR_WORKSPACE
     assert call_bwd(lib, ws_bytes=16) == evoattn.ERR_WORKSPACE
     assert call_bwd(lib, ws=ctypes.c_void_p((1 << 20) + 16)) == evoattn.ERR_WORKSPACE
@@ -138,6 +139,28 @@ def test_bf16_backward_d64_is_unsupported(lib):
     assert evoattn.workspace_size(1, 4, 2, 64, 64, torch_f32()) > 0
     # the forward accepts BF16 D = 64 (validation passes up to the alignment checks)
     assert call_fwd(lib, shape=shape, q=ctypes.c_void_p((1 << 20) + 8)) == evoattn.ERR_ALIGNMENT
+
+
+def test_deterministic_dq_workspace(lib):
+    """EVOATTN_DQ_DETERMINISTIC combines with either dbias mode; its BF16
+    workspace holds one fp32 dQ slice per 128-key tile instead of one, the
+    F32 workspace does not change, and an unknown bit makes the size query
+    return 0."""
+    B, S, H, N, D = 1, 8, 2, 300, 32
+    L = B * S * H * N * D
+    nkt = (N + 127) // 128
+    for dbias in (evoattn.DBIAS_DETERMINISTIC, evoattn.DBIAS_ATOMIC):
+        base = evoattn.workspace_size(B, S, H, N, D, flags=dbias)
+        det = evoattn.workspace_size(B, S, H, N, D, flags=dbias | evoattn.DQ_DETERMINISTIC)
+        assert det - base == (nkt - 1) * L * 4
+        assert call_bwd(lib, shape=(B, S, H, N, D), flags=dbias | evoattn.DQ_DETERMINISTIC,
+                        ws_bytes=det - 256) == \
+            evoattn.ERR_WORKSPACE
+    f32 = torch_f32()
+    assert evoattn.workspace_size(B, S, H, N, D, f32, flags=evoattn.DQ_DETERMINISTIC) == \
+        evoattn.workspace_size(B, S, H, N, D, f32)
+    assert evoattn.workspace_size(B, S, H, N, D, flags=4) == 0
+    assert call_bwd_noalloc(lib, flags=8) == evoattn.ERR_INVALID_ARG
 
 
 def test_debug_wait_hook_round_trips(lib):
