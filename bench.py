@@ -187,7 +187,9 @@ def measure_config(w, dev, peak, steps=5, warmup=3):
            "bwd_ms": t_b * 1e3, "bwd_tflops": w.bwd_flops / t_b / 1e12,
            "bwd_frac_of_peak": w.bwd_flops / t_b / 1e12 / peak,
            "L": w.B * w.S * w.H * w.N * w.D, "BHN2": w.B * w.H * w.N * w.N,
-           "device_bytes": held, "bwd_workspace_bytes": int(wsp.numel()),
+           "device_bytes": held,
+           "formula_bytes": held_bytes(B, S, H, N, D, gate=w.gate, mask=w.mask != "none"),
+           "bwd_workspace_bytes": int(wsp.numel()),
            "logits_bytes_if_materialized_bf16": int(w.logits * 2)}
     del x, out, lse, g, dbias, wsp
     torch.cuda.synchronize(dev)
@@ -228,19 +230,64 @@ def measure_ln_proj(N, dev, peaks, steps=10, warmup=3, B=1, C=128, H=4, D=32):
             "normalised_tensor_bytes_not_written": rows * C * 2}
 
 
+def held_bytes(B, S, H, N, D, gate=True, mask=True, flags=0):
+    """Device bytes a caller holds for one bf16 forward + backward: q, k, v,
+    dout (+ gate) and out, dq, dk, dv (+ dgate) [B,S,H,N,D]; the pair bias
+    (bf16) and dbias (fp32) [B,H,N,N]; the mask [B,S,N] (uint8); lse [B,S,H,N]
+    (fp32); the backward workspace the library asks for.  The library itself
+    allocates nothing."""
+    from protein_folding_attention_gb300 import evoattn
+    L, R, n2 = B * S * H * N * D, B * S * H * N, B * H * N * N
+    per_row_tensors = 4 + int(gate)
+    return (2 * per_row_tensors * L * 2 + n2 * 2 + n2 * 4 + (B * S * N if mask else 0) + R * 4
+            + evoattn.workspace_size(B, S, H, N, D, flags=flags))
+
+
+def dbias_slot_elems(B, S, H, N):
+    """Elements of the dbias slot partials in the backward workspace: the
+    slot count is about 4 * 152 / (B * H * tiles^2), at most S, so this term
+    stays below ~(608 + B*H*tiles^2) * 128^2 elements whatever S."""
+    nt = (N + 127) // 128
+    slots = min(S, max(1, -(-4 * 152 // (B * H * nt * nt))))
+    return slots * B * H * N * N
+
+
 def memory_fit(points):
-    """Least-squares fit of device bytes = a*L + b*BHN2 + c over the given
-    {"L", "BHN2", "device_bytes"} points (L = B*S*H*N*D, BHN2 = B*H*N*N).
-    Returns the coefficients and the largest relative residual."""
+    """Least-squares fit of held bytes = a*L + r*R + b*BHN2 + c*BSN + p*P + d*X
+    + e over {"L", "R", "BHN2", "BSN", "P", "X", "device_bytes"} points
+    (L = B*S*H*N*D, R = B*S*H*N rows, BHN2 = B*H*N*N, BSN = B*S*N, P = the
+    dbias slot-partial elements, X = B*S*H*N*N the logits).  A footprint linear in the inputs gives d = 0
+    and a zero residual.  Columns are scaled to unit norm before the solve."""
     import numpy as np
-    A = np.array([[p["L"], p["BHN2"], 1.0] for p in points], dtype=np.float64)
+    A = np.array([[p["L"], p["R"], p["BHN2"], p["BSN"], p["P"], p["X"], 1.0] for p in points],
+                 dtype=np.float64)
     y = np.array([p["device_bytes"] for p in points], dtype=np.float64)
-    coef, *_ = np.linalg.lstsq(A, y, rcond=None)
+    scale = np.linalg.norm(A, axis=0)
+    coef, *_ = np.linalg.lstsq(A / scale, y, rcond=None)
+    coef = coef / scale
     resid = A @ coef - y
-    return {"bytes_per_L": float(coef[0]), "bytes_per_BHN2": float(coef[1]),
-            "const_bytes": float(coef[2]),
+    return {"bytes_per_L": float(coef[0]), "bytes_per_row": float(coef[1]),
+            "bytes_per_BHN2": float(coef[2]), "bytes_per_BSN": float(coef[3]),
+            "bytes_per_slot_partial": float(coef[4]), "bytes_per_logit": float(coef[5]),
+            "const_bytes": float(coef[6]),
             "max_rel_residual": float(np.max(np.abs(resid) / y)),
             "points": len(points)}
+
+
+def memory_model(B=1):
+    """held_bytes over a grid of S, N (S = N and S != N, N off and on the
+    128-key tile size), H and D, and its fit: the linear footprint of the
+    library (bytes per L, per B*H*N^2, per mask byte, per dbias slot-partial
+    element) and the coefficient of the logits count, which must be zero."""
+    pts = []
+    for S in (16, 64, 256, 768, 1536):
+        for N in (64, 200, 384, 768, 1536):
+            for H, D in ((4, 32), (1, 16), (2, 32)):
+                pts.append({"L": B * S * H * N * D, "R": B * S * H * N,
+                            "BHN2": B * H * N * N, "BSN": B * S * N,
+                            "P": dbias_slot_elems(B, S, H, N), "X": B * S * H * N * N,
+                            "device_bytes": held_bytes(B, S, H, N, D)})
+    return memory_fit(pts)
 
 
 def oracle_sample_time(w, n_rows, device_inputs=None):
@@ -572,7 +619,7 @@ def run_ours(args, w):
         per_config = {}
         for name in PER_CONFIG:
             per_config[name] = measure_config(synthetic.WORKLOADS[name], dev, peak)
-        per_config["memory_fit"] = memory_fit([per_config[n] for n in PER_CONFIG])
+        per_config["memory_fit"] = memory_model()
     evofusion = None
     if rank == 0 and not args.no_per_config:
         evofusion = {f"n{n}": measure_ln_proj(n, dev, peaks) for n in (384, 768)}

@@ -286,7 +286,7 @@ struct DkdvCfg : Tile<D> {
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory overflow");
   static_assert(OFF_BIAS % 1024 == 0 && OFF_DS % 1024 == 0 && OFF_Z % 256 == 0, "alignment");
   static constexpr int THREADS = 384;
-  static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 224;
+  static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 216;
   static_assert(REGS_LOW * 128 + REGS_HIGH * 256 <= LAUNCH_REGS * THREADS, "register split");
 };
 

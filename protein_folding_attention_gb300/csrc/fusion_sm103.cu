@@ -65,7 +65,7 @@ struct FusionCfg {
   static constexpr uint32_t SMEM = OFF_STAGE + 4 * 32 * 128;
   static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
   static constexpr int THREADS = 384;
-  static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_LN = 232, REGS_EPI = 216;
+  static constexpr int LAUNCH_REGS = 168, REGS_LOW = 64, REGS_LN = 224, REGS_EPI = 216;
   static_assert(REGS_LOW + REGS_LN + REGS_EPI <= 3 * LAUNCH_REGS, "register split");
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory");
 };

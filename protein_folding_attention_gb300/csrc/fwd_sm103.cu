@@ -85,7 +85,7 @@ struct FwdCfg {
   static constexpr int THREADS = 384;
   // register split: launch 168/thread; the producer warpgroup drops to 80,
   // the softmax warpgroups rise to 208 (80*128 + 208*256 <= 168*384)
-  static constexpr int LAUNCH_REGS = 168, REGS_LOW = 80, REGS_HIGH = 208;
+  static constexpr int LAUNCH_REGS = 168, REGS_LOW = 104, REGS_HIGH = 192;
   static_assert(REGS_LOW * 128 + REGS_HIGH * 256 <= LAUNCH_REGS * THREADS, "register split");
   static_assert(NT * 128 <= TMEM_O && TMEM_O + G * D <= TMEM_COLS, "tensor memory overflow");
   static_assert(OFF_BIAS % 1024 == 0 && OFF_Z % 256 == 0, "operand alignment");

@@ -67,15 +67,41 @@ def test_reference_arm_json_line():
 
 
 def test_memory_fit_recovers_a_linear_footprint():
-    """The fit of held device bytes against L = B*S*H*N*D and B*H*N^2 returns
-    the coefficients of an exactly linear footprint and a zero residual; a
-    cubic term shows up as a large residual."""
+    """The fit of held device bytes returns the coefficients of a footprint
+    that is linear in its inputs and a zero residual; a term in the logits
+    count X = B*S*H*N^2 shows up as its own coefficient."""
     pts = []
-    for L, n2 in ((100, 10), (800, 40), (6400, 160), (3000, 90)):
-        pts.append({"L": L, "BHN2": n2, "device_bytes": 26 * L + 6 * n2 + 1000})
+    for B, S, H, N, D in ((1, 8, 2, 64, 32), (1, 64, 4, 200, 16), (2, 16, 1, 384, 32),
+                          (1, 300, 4, 96, 32), (1, 5, 2, 768, 16), (3, 40, 2, 128, 32),
+                          (1, 1, 8, 1000, 16), (1, 77, 3, 333, 32)):
+        p = {"L": B * S * H * N * D, "R": B * S * H * N, "BHN2": B * H * N * N,
+             "BSN": B * S * N, "P": bench.dbias_slot_elems(B, S, H, N),
+             "X": B * S * H * N * N}
+        p["device_bytes"] = (26 * p["L"] + 8 * p["R"] + 6 * p["BHN2"] + p["BSN"]
+                             + 4 * p["P"] + 1000)
+        pts.append(p)
     f = bench.memory_fit(pts)
     assert f["bytes_per_L"] == pytest.approx(26.0)
     assert f["bytes_per_BHN2"] == pytest.approx(6.0)
+    assert abs(f["bytes_per_logit"]) < 1e-9
     assert f["max_rel_residual"] < 1e-9
-    cubic = [dict(p, device_bytes=p["device_bytes"] + p["L"] ** 1.5) for p in pts]
-    assert bench.memory_fit(cubic)["max_rel_residual"] > 1e-2
+    cubic = [dict(p, device_bytes=p["device_bytes"] + 2 * p["X"]) for p in pts]
+    assert bench.memory_fit(cubic)["bytes_per_logit"] == pytest.approx(2.0)
+
+
+def test_library_footprint_has_no_logit_term():
+    """What a caller holds for one forward + backward (inputs, outputs and the
+    workspace the library asks for; the library allocates nothing), over a
+    grid of S, N, H and D: exactly 26 bytes per element of q (ten bf16
+    tensors, the bf16 gated output gradient, the fp32 dQ accumulator), 8 per
+    query row (lse, delta), 6 per pair-bias entry (bf16 bias, fp32 dbias), 1
+    per mask byte and 4 per dbias slot-partial element, and nothing per
+    logit."""
+    f = bench.memory_model()
+    assert f["max_rel_residual"] < 1e-9
+    assert f["bytes_per_L"] == pytest.approx(26.0)
+    assert f["bytes_per_row"] == pytest.approx(8.0)
+    assert f["bytes_per_BHN2"] == pytest.approx(6.0)
+    assert f["bytes_per_BSN"] == pytest.approx(1.0)
+    assert f["bytes_per_slot_partial"] == pytest.approx(4.0)
+    assert abs(f["bytes_per_logit"]) < 1e-9
