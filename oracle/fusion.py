@@ -1,9 +1,11 @@
-"""EvoFusion upstream oracle -- test infrastructure only.
+"""EvoFusion oracles -- test infrastructure only.
 
-A plain float64 CPU statement of the operator stack that feeds triangle
-attention: LayerNorm of the pair representation over its channel axis, then
-one linear projection without a bias term whose output columns are the
-queries, keys, values and gate of every head and the pair bias of every head.
+Plain float64 CPU statements of the operator stacks around triangle
+attention.  Upstream: LayerNorm of the pair representation over its channel
+axis, then one linear projection without a bias term whose output columns
+are the queries, keys, values and gate of every head and the pair bias of
+every head.  Downstream: the SwiGLU transition of the pair representation
+with its residual add.
 
 MegaFold technical summary, "Methodik" section 3 "EvoFusion", Umfang and
 Mechanismus: EvoFusion restructures layer normalisation and the linear
@@ -18,6 +20,14 @@ compute exactly this up to its stated rounding.
 Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this module.  The product library never does, and
 this module imports nothing from the product.
+
+The downstream stack is named in the same passage (Umfang: layer
+normalisation, linear projections and SwiGLU activations).  The pages print
+no formula for it either; the plainest reading, taken here, is the
+transition block of AlphaFold3-style pair stacks: LayerNorm as above, two
+bias-free projections to F hidden units (a SiLU branch and a linear
+branch), their product, a bias-free projection back to C channels, and the
+residual add of the block's input.
 
 Parity status: pinned (tests/test_fusion_oracle_pins.py).
 """
@@ -64,3 +74,32 @@ def ln_proj(z, gamma, beta, w, H, D, eps=1e-5):
     parts = [out[:, i * hd:(i + 1) * hd].reshape(B, N, N, H, D) for i in range(4)]
     bias = out[:, 4 * hd:].reshape(B, N, N, H).transpose(0, 3, 1, 2).copy()
     return parts[0], parts[1], parts[2], parts[3], bias
+
+
+def silu(x):
+    """x * sigmoid(x) = x / (1 + exp(-x)), written so that it does not
+    overflow for large negative x."""
+    x = _f64(x)
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, x / (1.0 + e), x * e / (1.0 + e))
+
+
+def transition(z, gamma, beta, w1, w2, eps=1e-5):
+    """The SwiGLU transition of the pair representation, with its residual.
+
+    z      : [B, N, N, C] pair representation.
+    gamma, beta : [C] LayerNorm scale and shift.
+    w1     : [2F, C]: rows 0..F-1 the SiLU branch, rows F..2F-1 the linear branch.
+    w2     : [C, F].
+    Returns float64 out [B, N, N, C] = z + (silu(y w1a^T) * (y w1b^T)) w2^T,
+    y = LayerNorm(z).
+    """
+    z = _f64(z)
+    y = layer_norm(z, gamma, beta, eps)
+    w1, w2 = _f64(w1), _f64(w2)
+    F = w1.shape[0] // 2
+    assert w1.shape == (2 * F, z.shape[-1]) and w2.shape == (z.shape[-1], F)
+    a = y @ w1[:F].T
+    b = y @ w1[F:].T
+    h = silu(a) * b
+    return z + h @ w2.T

@@ -177,3 +177,23 @@ def make_fusion_inputs(B, N, C, H, D, seed=0, device="cpu"):
     beta = 0.1 * torch.randn(C, generator=gen, **f32)
     w = (torch.randn(4 * H * D + H, C, generator=gen, **f32) * C ** -0.5).to(torch.bfloat16)
     return {"z": z, "gamma": gamma, "beta": beta, "w": w}
+
+
+def make_transition_inputs(B, N, C, F, seed=0, device="cpu"):
+    """Seeded inputs of the EvoFusion downstream stack (the SwiGLU transition
+    with its residual add): z [B, N, N, C] bf16 with a per-channel offset and
+    scale, gamma ~ 1 + 0.1 N(0,1) and beta ~ 0.1 N(0,1) in fp32, w1 [2F, C]
+    bf16 ~ N(0, 1/C) (so the SiLU and linear branches are of order one) and
+    w2 [C, F] bf16 ~ N(0, 1/F).  Draw order: channel offsets, channel scales,
+    z, gamma, beta, w1, w2."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    f32 = dict(device=device, dtype=torch.float32)
+    mu = torch.randn(C, generator=gen, **f32)
+    sd = torch.rand(C, generator=gen, **f32) * 1.5 + 0.5
+    z = (torch.randn(B, N, N, C, generator=gen, **f32) * sd + mu).to(torch.bfloat16)
+    gamma = 1.0 + 0.1 * torch.randn(C, generator=gen, **f32)
+    beta = 0.1 * torch.randn(C, generator=gen, **f32)
+    w1 = (torch.randn(2 * F, C, generator=gen, **f32) * C ** -0.5).to(torch.bfloat16)
+    w2 = (torch.randn(C, F, generator=gen, **f32) * F ** -0.5).to(torch.bfloat16)
+    return {"z": z, "gamma": gamma, "beta": beta, "w1": w1, "w2": w2}
