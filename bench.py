@@ -230,6 +230,43 @@ def measure_ln_proj(N, dev, peaks, steps=10, warmup=3, B=1, C=128, H=4, D=32):
             "normalised_tensor_bytes_not_written": rows * C * 2}
 
 
+def measure_transition(N, dev, peaks, steps=10, warmup=3, B=1, C=128, F=512, HD=0):
+    """The EvoFusion downstream stack (the SwiGLU transition with its residual
+    add) on the [B, N, N, C] pair representation: CUDA-event time, TFLOP/s of
+    the two projections against the measured bf16 peak, and the HBM rate of
+    its algorithmic bytes (z read, out written; the 384 KB of weights come
+    from L2)."""
+    import torch
+
+    from protein_folding_attention_gb300 import evoattn, synthetic
+    x = synthetic.make_transition_inputs(B, N, C, F, seed=N, device=dev, HD=HD)
+    run = lambda out=None: evoattn.transition(x["z"], x["gamma"], x["beta"], x["w1"], x["w2"],
+                                              o=x["o"], w_o=x["w_o"], out=out)
+    out = run()
+    for _ in range(warmup):
+        run(out)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        a.record()
+        run(out)
+        b.record()
+    torch.cuda.synchronize(dev)
+    if evoattn.device_status() != evoattn.OK:
+        raise RuntimeError("device status set by evoattn_transition")
+    t = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e-3
+    rows = B * N * N
+    flops = 6 * rows * C * F + 2 * rows * C * HD
+    bytes_ = 2 * rows * C * 2 + rows * HD * 2 + (3 * F + HD) * C * 2
+    name = f"pair_outproj_transition_n{N}" if HD else f"pair_transition_n{N}"
+    return {"workload": name, "B": B, "N": N, "C": C, "F": F, "HD": HD,
+            "ms": t * 1e3, "tflops": flops / t / 1e12,
+            "frac_of_bf16_peak": flops / t / 1e12 / peaks["bf16_tflops"],
+            "hbm_bytes": bytes_, "hbm_gbs": bytes_ / t / 1e9,
+            "traffic": profiled_traffic("evoattn_transition_kernel", name),
+            "intermediate_bytes_not_written": rows * ((2 if HD else 1) * C + 3 * F) * 2}
+
+
 def held_bytes(B, S, H, N, D, gate=True, mask=True, flags=0):
     """Device bytes a caller holds for one bf16 forward + backward: q, k, v,
     dout (+ gate) and out, dq, dk, dv (+ dgate) [B,S,H,N,D]; the pair bias
@@ -623,6 +660,10 @@ def run_ours(args, w):
     evofusion = None
     if rank == 0 and not args.no_per_config:
         evofusion = {f"n{n}": measure_ln_proj(n, dev, peaks) for n in (384, 768)}
+        evofusion.update({f"transition_n{n}": measure_transition(n, dev, peaks)
+                          for n in (384, 768)})
+        evofusion.update({f"outproj_transition_n{n}": measure_transition(n, dev, peaks, HD=128)
+                          for n in (384, 768)})
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
@@ -693,7 +734,18 @@ def main():
     ap.add_argument("--evofusion-only", type=int, default=0, metavar="N",
                     help="profiling only: time the LayerNorm + projection kernel on the "
                          "[1, N, N, 128] pair representation and print its JSON")
+    ap.add_argument("--transition-only", type=int, default=0, metavar="N",
+                    help="profiling only: time the fused SwiGLU transition kernel on the "
+                         "[1, N, N, 128] pair representation and print its JSON")
     args = ap.parse_args()
+    if args.transition_only:
+        import torch
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        peaks, _ = load_peaks()
+        print(json.dumps(measure_transition(args.transition_only, dev, peaks)))
+        print(json.dumps(measure_transition(args.transition_only, dev, peaks, HD=128)))
+        return 0
     if args.evofusion_only:
         import torch
         dev = torch.device("cuda", 0)

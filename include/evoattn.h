@@ -295,7 +295,7 @@ evoattn_status evoattn_get_device_status(cudaStream_t stream, int* device_status
  *               (the pair projections in the layout the attention reads as
  *               starting- or ending-node views).
  *  pair_bias  : [B, H, N, N] device bf16, dense, written.
- * Supported: C = 128, H * D = 128, H <= 8, B * N * N < 2^31 (otherwise
+ * Supported: C = 128, H * D = 128, H <= 8, B * N * N < 2^31 - 128 (otherwise
  * EVOATTN_ERR_UNSUPPORTED).  g is the gate's pre-activation: the attention
  * applies the sigmoid.  Returns EVOATTN_OK once the kernel is enqueued.
  */
@@ -303,6 +303,44 @@ evoattn_status evoattn_ln_proj(const void* z, const float* gamma, const float* b
                                const void* w, float eps,
                                void* q, void* k, void* v, void* g, void* pair_bias,
                                int B, int N, int C, int H, int D, cudaStream_t stream);
+
+/*
+ * The operators that follow the gated attention in a pair-stack block, as one
+ * fused operator (MegaFold technical summary, "Methodik" section 3
+ * "EvoFusion", Umfang: layer normalisation, linear projections and SwiGLU
+ * activations; Mechanismus: no intermediate N x N tensor is written to HBM
+ * between them): the attention's output projection with its residual add
+ * (when o is given), then the SwiGLU transition with its residual add.  For
+ * every row r = (b, i, j), with F hidden units:
+ *
+ *   z1[r, c]  = z[r, c] + sum_e o[r, e] w_o[c, e]        (fp32; z1 = z without o)
+ *   y[r, c]   = bf16((z1[r, c] - mean_c z1[r, :]) / sqrt(var_c z1[r, :] + eps)
+ *                    * gamma[c] + beta[c])          (var: mean squared deviation)
+ *   a[r, f]   = sum_c y[r, c] w1[f, c],   b[r, f] = sum_c y[r, c] w1[F + f, c]
+ *   h[r, f]   = bf16(silu(a[r, f]) * b[r, f]),   silu(x) = x / (1 + exp(-x))
+ *   out[r, c] = bf16(z1[r, c] + sum_f h[r, f] w2[c, f])    (fp32 sums)
+ *
+ *  z          : [B, N, N, C] device bf16, dense (C contiguous), 16-byte aligned.
+ *  o          : [B, N, N, HD] device bf16, dense, 16-byte aligned: the gated
+ *               attention output of the same rows (evoattn_fwd's out, stored
+ *               with (b, i, j) outermost); NULL for the transition alone.
+ *  w_o        : [C, HD] device bf16, dense row-major, 16-byte aligned; NULL
+ *               exactly when o is NULL.
+ *  gamma, beta: [C] device fp32.
+ *  w1         : [2F, C] device bf16, dense row-major, 16-byte aligned (rows
+ *               0..F-1 the SiLU branch, F..2F-1 the linear branch).
+ *  w2         : [C, F] device bf16, dense row-major, 16-byte aligned.
+ *  eps        : > 0, added to the variance.
+ *  out        : [B, N, N, C] device bf16, dense, 16-byte aligned, written; it
+ *               may not overlap z or o.
+ * Supported: C = 128, HD = 128 (with o), F = 4C, B * N * N < 2^31 - 128
+ * (otherwise EVOATTN_ERR_UNSUPPORTED).  Returns EVOATTN_OK once the kernel is
+ * enqueued.
+ */
+evoattn_status evoattn_transition(const void* z, const void* o, const void* w_o,
+                                  const float* gamma, const float* beta,
+                                  const void* w1, const void* w2, float eps, void* out,
+                                  int B, int N, int C, int HD, int F, cudaStream_t stream);
 
 /*
  * Testing hook for the bounded-wait failure path; not needed in normal use.

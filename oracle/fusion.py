@@ -23,11 +23,13 @@ this module imports nothing from the product.
 
 The downstream stack is named in the same passage (Umfang: layer
 normalisation, linear projections and SwiGLU activations).  The pages print
-no formula for it either; the plainest reading, taken here, is the
-transition block of AlphaFold3-style pair stacks: LayerNorm as above, two
-bias-free projections to F hidden units (a SiLU branch and a linear
-branch), their product, a bias-free projection back to C channels, and the
-residual add of the block's input.
+no formula for it either; the plainest reading, taken here, is what follows
+the gated attention in AlphaFold3-style pair stacks: the attention's
+bias-free output projection from H*D back to C channels and its residual add,
+then the transition block -- LayerNorm as above, two bias-free projections to
+F hidden units (a SiLU branch and a linear branch), their product, a
+bias-free projection back to C channels, and the residual add of the
+block's input.
 
 Parity status: pinned (tests/test_fusion_oracle_pins.py).
 """
@@ -84,17 +86,23 @@ def silu(x):
     return np.where(x >= 0, x / (1.0 + e), x * e / (1.0 + e))
 
 
-def transition(z, gamma, beta, w1, w2, eps=1e-5):
-    """The SwiGLU transition of the pair representation, with its residual.
+def transition(z, gamma, beta, w1, w2, eps=1e-5, o=None, w_o=None):
+    """The output projection of the gated attention with its residual add
+    (when o is given), then the SwiGLU transition with its residual add.
 
     z      : [B, N, N, C] pair representation.
+    o      : [B, N, N, HD] gated attention output of the same rows (optional).
+    w_o    : [C, HD] output projection (given exactly when o is).
     gamma, beta : [C] LayerNorm scale and shift.
     w1     : [2F, C]: rows 0..F-1 the SiLU branch, rows F..2F-1 the linear branch.
     w2     : [C, F].
-    Returns float64 out [B, N, N, C] = z + (silu(y w1a^T) * (y w1b^T)) w2^T,
-    y = LayerNorm(z).
+    Returns float64 out [B, N, N, C] = z1 + (silu(y w1a^T) * (y w1b^T)) w2^T,
+    y = LayerNorm(z1), z1 = z + o w_o^T (z1 = z without o).
     """
     z = _f64(z)
+    assert (o is None) == (w_o is None)
+    if o is not None:
+        z = z + _f64(o) @ _f64(w_o).T
     y = layer_norm(z, gamma, beta, eps)
     w1, w2 = _f64(w1), _f64(w2)
     F = w1.shape[0] // 2

@@ -17,7 +17,7 @@ OBJDIR = os.path.join(ROOT, "_build", "evoattn")
 LIB = os.path.join(HERE, "libevoattn.so")
 
 SOURCES = ["evoattn_api.cu", "simt_f32.cu", "tmap.cu", "fwd_sm103.cu", "bwd_sm103.cu",
-           "fusion_sm103.cu", "evoattn_noalloc.cu"]
+           "fusion_sm103.cu", "transition_sm103.cu", "evoattn_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + INCLUDE, "-I" + CSRC]

@@ -145,7 +145,7 @@ evoattn_status evoattn_ln_proj(const void* z, const float* gamma, const float* b
   if (B < 1 || N < 1 || C < 1 || H < 1 || D < 1) return EVOATTN_ERR_INVALID_ARG;
   if (!(eps > 0.f) || !(eps < INFINITY)) return EVOATTN_ERR_INVALID_ARG;
   if (C != 128 || H * D != 128 || H > 8) return EVOATTN_ERR_UNSUPPORTED;
-  if ((uint64_t)B * N * N > 0x7FFFFFFFull) return EVOATTN_ERR_UNSUPPORTED;
+  if ((uint64_t)B * N * N + 128 > 0x7FFFFFFFull) return EVOATTN_ERR_UNSUPPORTED;
   auto a16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
   if (!a16(z) || !a16(w) || !a16(q) || !a16(k) || !a16(v) || !a16(g) ||
       reinterpret_cast<uintptr_t>(gamma) % 4 || reinterpret_cast<uintptr_t>(beta) % 4 ||
@@ -157,6 +157,30 @@ evoattn_status evoattn_ln_proj(const void* z, const float* gamma, const float* b
   bool tmap_ok = true;
   cudaError_t e = bf16_ln_proj(z, gamma, beta, w, eps, q, k, v, g, pair_bias, B, N, H,
                                wait_base(status), stream, &tmap_ok);
+  if (!tmap_ok) return EVOATTN_ERR_ALIGNMENT;
+  return cuda_status(e);
+}
+
+evoattn_status evoattn_transition(const void* z, const void* o, const void* w_o,
+                                  const float* gamma, const float* beta, const void* w1,
+                                  const void* w2, float eps, void* out, int B, int N, int C,
+                                  int HD, int F, cudaStream_t stream) {
+  if (!z || !gamma || !beta || !w1 || !w2 || !out) return EVOATTN_ERR_INVALID_ARG;
+  if ((o == nullptr) != (w_o == nullptr)) return EVOATTN_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || C < 1 || F < 1 || (o && HD < 1)) return EVOATTN_ERR_INVALID_ARG;
+  if (!(eps > 0.f) || !(eps < INFINITY)) return EVOATTN_ERR_INVALID_ARG;
+  if (C != 128 || F != 4 * C || (o && HD != 128)) return EVOATTN_ERR_UNSUPPORTED;
+  if ((uint64_t)B * N * N + 128 > 0x7FFFFFFFull) return EVOATTN_ERR_UNSUPPORTED;
+  auto a16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+  if (!a16(z) || !a16(w1) || !a16(w2) || !a16(out) || !a16(o) || !a16(w_o) ||
+      reinterpret_cast<uintptr_t>(gamma) % 4 || reinterpret_cast<uintptr_t>(beta) % 4)
+    return EVOATTN_ERR_ALIGNMENT;
+  bool ok = false;
+  unsigned int* status = status_word(&ok);
+  if (!ok) return EVOATTN_ERR_CUDA;
+  bool tmap_ok = true;
+  cudaError_t e = bf16_transition(z, o, w_o, gamma, beta, w1, w2, eps, out, B, N,
+                                  wait_base(status), stream, &tmap_ok);
   if (!tmap_ok) return EVOATTN_ERR_ALIGNMENT;
   return cuda_status(e);
 }

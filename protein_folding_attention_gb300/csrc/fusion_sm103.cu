@@ -82,25 +82,6 @@ struct FusionParams {
   WaitCfg wc;
 };
 
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int c0,
-                                             int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-          reinterpret_cast<uint64_t>(m)),
-      "r"(c0), "r"(c1), "r"(smem_u32(src))
-      : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// The staging buffer may be rewritten once the bulk stores committed so far
-// have read it.
-__device__ __forceinline__ void tma_store_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Every bulk store committed so far has completed.
-__device__ __forceinline__ void tma_store_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 __global__ void __launch_bounds__(384, 1)
     evoattn_ln_proj_kernel(const __grid_constant__ CUtensorMap tm_z,
                            const __grid_constant__ CUtensorMap tm_w,

@@ -39,6 +39,13 @@ cudaError_t bf16_ln_proj(const void* z, const float* gamma, const float* beta, c
                          float eps, void* q, void* k, void* v, void* g, void* bias, int B, int N,
                          int H, const WaitCfg& wait, cudaStream_t st, bool* tmap_ok);
 
+// Output projection (o and w_o nullable together) + SwiGLU transition
+// (EvoFusion downstream); C = 128, H * D = 128, F = 4C.
+cudaError_t bf16_transition(const void* z, const void* o, const void* w_o, const float* gamma,
+                            const float* beta, const void* w1, const void* w2, float eps,
+                            void* out, int B, int N, const WaitCfg& wait, cudaStream_t st,
+                            bool* tmap_ok);
+
 size_t bf16_bwd_workspace_bytes(const Problem& P, unsigned flags);
 // `events` (nullable): 5 caller-owned events recorded around the stages.
 cudaError_t bf16_bwd(const Problem& P, const Bf16Ptrs& a, unsigned flags, void* ws,

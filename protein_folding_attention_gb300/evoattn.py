@@ -64,6 +64,9 @@ def load(path: str = LIB_PATH):
     lib.evoattn_ln_proj.argtypes = [vp, fp, fp, vp, ctypes.c_float, vp, vp, vp, vp, vp,
                                     i, i, i, i, i, vp]
     lib.evoattn_ln_proj.restype = i
+    lib.evoattn_transition.argtypes = [vp, vp, vp, fp, fp, vp, vp, ctypes.c_float, vp,
+                                       i, i, i, i, i, vp]
+    lib.evoattn_transition.restype = i
     lib.evoattn_debug_set_wait.argtypes = [ctypes.c_ulonglong, i]
     lib.evoattn_debug_set_wait.restype = i
     _lib = lib
@@ -203,6 +206,27 @@ def ln_proj(z, gamma, beta, w, H, D, eps=1e-5, out=None, stream=None):
                              B, N, C, H, D, _stream(stream))
     _check(st, "evoattn_ln_proj")
     return q, k, v, g, bias
+
+
+def transition(z, gamma, beta, w1, w2, eps=1e-5, o=None, w_o=None, out=None, stream=None):
+    """EvoFusion downstream stack: z1 = z + o w_o^T (when o is given), then
+    out = z1 + SwiGLU transition of LayerNorm(z1), for z [B, N, N, C] (bf16,
+    dense), o [B, N, N, HD] and w_o [C, HD] (bf16), gamma, beta [C] (fp32),
+    w1 [2F, C] and w2 [C, F] (bf16).  Returns out [B, N, N, C] bf16 (see
+    evoattn_transition)."""
+    lib = load()
+    B, N, N2, C = z.shape
+    if N2 != N:
+        raise ValueError("z must be [B, N, N, C]")
+    F = w2.shape[1]
+    HD = o.shape[-1] if o is not None else 0
+    if out is None:
+        out = torch.empty_like(z)
+    st = lib.evoattn_transition(_ptr(z), _ptr(o), _ptr(w_o), _ptr(gamma), _ptr(beta),
+                                _ptr(w1), _ptr(w2), float(eps), _ptr(out), B, N, C, HD, F,
+                                _stream(stream))
+    _check(st, "evoattn_transition")
+    return out
 
 
 def debug_set_wait(limit_ns: int = 0, stall: bool = False) -> None:

@@ -179,13 +179,16 @@ def make_fusion_inputs(B, N, C, H, D, seed=0, device="cpu"):
     return {"z": z, "gamma": gamma, "beta": beta, "w": w}
 
 
-def make_transition_inputs(B, N, C, F, seed=0, device="cpu"):
+def make_transition_inputs(B, N, C, F, seed=0, device="cpu", HD=0):
     """Seeded inputs of the EvoFusion downstream stack (the SwiGLU transition
-    with its residual add): z [B, N, N, C] bf16 with a per-channel offset and
-    scale, gamma ~ 1 + 0.1 N(0,1) and beta ~ 0.1 N(0,1) in fp32, w1 [2F, C]
-    bf16 ~ N(0, 1/C) (so the SiLU and linear branches are of order one) and
-    w2 [C, F] bf16 ~ N(0, 1/F).  Draw order: channel offsets, channel scales,
-    z, gamma, beta, w1, w2."""
+    with its residual add, optionally preceded by the attention's output
+    projection): z [B, N, N, C] bf16 with a per-channel offset and scale,
+    gamma ~ 1 + 0.1 N(0,1) and beta ~ 0.1 N(0,1) in fp32, w1 [2F, C] bf16
+    ~ N(0, 1/C) (so the SiLU and linear branches are of order one), w2 [C, F]
+    bf16 ~ N(0, 1/F) and, when HD > 0, the gated attention output o
+    [B, N, N, HD] bf16 ~ N(0, 1/4) (the size of a gated, averaged value) and
+    w_o [C, HD] bf16 ~ N(0, 1/HD).  Draw order: channel offsets, channel
+    scales, z, gamma, beta, w1, w2, o, w_o."""
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     f32 = dict(device=device, dtype=torch.float32)
@@ -196,4 +199,8 @@ def make_transition_inputs(B, N, C, F, seed=0, device="cpu"):
     beta = 0.1 * torch.randn(C, generator=gen, **f32)
     w1 = (torch.randn(2 * F, C, generator=gen, **f32) * C ** -0.5).to(torch.bfloat16)
     w2 = (torch.randn(C, F, generator=gen, **f32) * F ** -0.5).to(torch.bfloat16)
-    return {"z": z, "gamma": gamma, "beta": beta, "w1": w1, "w2": w2}
+    x = {"z": z, "gamma": gamma, "beta": beta, "w1": w1, "w2": w2, "o": None, "w_o": None}
+    if HD > 0:
+        x["o"] = (torch.randn(B, N, N, HD, generator=gen, **f32) * 0.5).to(torch.bfloat16)
+        x["w_o"] = (torch.randn(C, HD, generator=gen, **f32) * HD ** -0.5).to(torch.bfloat16)
+    return x

@@ -205,3 +205,28 @@ def test_ln_proj_rejects_bad_arguments(lib):
     assert call_ln_proj(lib, B=1, N=50000) == evoattn.ERR_UNSUPPORTED  # B*N*N >= 2^31
     assert call_ln_proj(lib, z=ctypes.c_void_p((1 << 20) + 8)) == evoattn.ERR_ALIGNMENT
     assert call_ln_proj(lib, w=ctypes.c_void_p((1 << 20) + 2)) == evoattn.ERR_ALIGNMENT
+
+
+def call_transition(lib, *, z=FAKE, o=None, w_o=None, w1=FAKE, w2=FAKE, out=FAKE, eps=1e-5,
+                    B=1, N=8, C=128, HD=128, F=512):
+    return lib.evoattn_transition(z, o, w_o, FAKE, FAKE, w1, w2, eps, out, B, N, C, HD, F, None)
+
+
+def test_transition_rejects_bad_arguments(lib):
+    assert call_transition(lib, z=None) == evoattn.ERR_INVALID_ARG
+    assert call_transition(lib, w2=None) == evoattn.ERR_INVALID_ARG
+    assert call_transition(lib, out=None) == evoattn.ERR_INVALID_ARG
+    assert call_transition(lib, o=FAKE) == evoattn.ERR_INVALID_ARG        # o without w_o
+    assert call_transition(lib, w_o=FAKE) == evoattn.ERR_INVALID_ARG      # w_o without o
+    assert call_transition(lib, N=0) == evoattn.ERR_INVALID_ARG
+    assert call_transition(lib, eps=0.0) == evoattn.ERR_INVALID_ARG
+    assert call_transition(lib, eps=float("inf")) == evoattn.ERR_INVALID_ARG
+    assert call_transition(lib, C=64, F=256) == evoattn.ERR_UNSUPPORTED
+    assert call_transition(lib, F=256) == evoattn.ERR_UNSUPPORTED    # F != 4C
+    assert call_transition(lib, o=FAKE, w_o=FAKE, HD=64) == evoattn.ERR_UNSUPPORTED
+    assert call_transition(lib, B=1, N=50000) == evoattn.ERR_UNSUPPORTED  # B*N*N >= 2^31
+    assert call_transition(lib, z=ctypes.c_void_p((1 << 20) + 8)) == evoattn.ERR_ALIGNMENT
+    assert call_transition(lib, w1=ctypes.c_void_p((1 << 20) + 2)) == evoattn.ERR_ALIGNMENT
+    assert call_transition(lib, out=ctypes.c_void_p((1 << 20) + 4)) == evoattn.ERR_ALIGNMENT
+    assert call_transition(lib, o=ctypes.c_void_p((1 << 20) + 8), w_o=FAKE) == \
+        evoattn.ERR_ALIGNMENT

@@ -1,6 +1,7 @@
 """Pins for the EvoFusion downstream oracle (oracle/fusion.py `transition`,
-`silu`): the SwiGLU transition of the pair representation with its residual
-add.  Checked without re-typing the oracle's formula:
+`silu`): the attention's output projection with its residual add, then the
+SwiGLU transition of the pair representation with its residual add.  Checked
+without re-typing the oracle's formula:
 * SiLU against its closed-form values (silu(0) = 0, silu(1) = e / (1 + e),
   silu(-1) = -1 / (1 + e)), the identity silu(x) - silu(-x) = x, and its
   limits (x for large x, 0 for large negative x, no overflow);
@@ -8,6 +9,9 @@ add.  Checked without re-typing the oracle's formula:
 * special cases: zero output weights, or a zero linear branch, return z
   exactly; the update out - z is linear in w2, ignores a per-row shift of z
   (the LayerNorm removes it), and rows are independent;
+* the output projection: a zero w_o changes nothing, a zero linear branch
+  leaves z + o w_o^T (checked against torch's float64 matmul), and a worked
+  row by hand;
 * an independent library: torch's float64 layer_norm, silu and matmul.
 """
 import math
@@ -96,3 +100,44 @@ def test_matches_torch_layer_norm_silu_and_matmul(eps):
     ref = (t(z) + h @ t(w2).T).numpy()
     np.testing.assert_allclose(fusion.transition(z, gamma, beta, w1, w2, eps), ref, rtol=1e-12,
                                atol=1e-12)
+
+
+def test_output_projection_by_hand():
+    """z = [1, 2], o = [1], w_o = [[0], [1]]: z1 = [1, 3], then the worked
+    transition above (y = [-1, 1], h = 3 e / (1 + e))."""
+    z = np.array([[[[1.0, 2.0]]]])
+    o = np.array([[[[1.0]]]])
+    w_o = np.array([[0.0], [1.0]])
+    w1 = np.array([[0.0, 1.0], [0.0, 3.0]])
+    w2 = np.array([[1.0], [-2.0]])
+    h = 3 * math.e / (1 + math.e)
+    out = fusion.transition(z, np.ones(2), np.zeros(2), w1, w2, eps=0.0, o=o, w_o=w_o)
+    np.testing.assert_allclose(out.reshape(2), [1.0 + h, 3.0 - 2 * h], rtol=0, atol=1e-14)
+
+
+def test_output_projection_special_cases():
+    z, gamma, beta, w1, w2 = _inputs(21, C=8, F=16)
+    o = _rand(z.shape[:-1] + (12,), 22)
+    w_o = _rand((8, 12), 23, 12 ** -0.5)
+    base = fusion.transition(z, gamma, beta, w1, w2)
+    assert np.array_equal(fusion.transition(z, gamma, beta, w1, w2, o=o, w_o=np.zeros_like(w_o)),
+                          base)
+    F = w2.shape[1]
+    w1b0 = w1.copy()
+    w1b0[F:] = 0.0
+    got = fusion.transition(z, gamma, beta, w1b0, w2, o=o, w_o=w_o)
+    ref = (torch.from_numpy(z) + torch.from_numpy(o) @ torch.from_numpy(w_o).T).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_with_output_projection_matches_torch():
+    z, gamma, beta, w1, w2 = _inputs(24, B=1, N=4, C=16, F=64)
+    o = _rand(z.shape[:-1] + (16,), 25, 0.5)
+    w_o = _rand((16, 16), 26, 0.25)
+    t = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
+    F = w2.shape[1]
+    z1 = t(z) + t(o) @ t(w_o).T
+    y = torch.nn.functional.layer_norm(z1, (16,), t(gamma), t(beta), 1e-5)
+    ref = (z1 + (torch.nn.functional.silu(y @ t(w1[:F]).T) * (y @ t(w1[F:]).T)) @ t(w2).T)
+    np.testing.assert_allclose(fusion.transition(z, gamma, beta, w1, w2, o=o, w_o=w_o),
+                               ref.numpy(), rtol=1e-12, atol=1e-12)

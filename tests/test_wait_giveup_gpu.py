@@ -91,3 +91,21 @@ def test_ln_proj_gives_up_and_recovers():
     ref = fusion.ln_proj(x["z"], x["gamma"], x["beta"], x["w"], 4, 32)
     for got, r in zip(out, ref):
         assert rel_l2(got, r) <= 5e-3
+
+
+def test_transition_gives_up_and_recovers():
+    """The fused transition kernel: its LayerNorm warps' first wait stalls,
+    every CTA gives up, the status reads ERR_TIMEOUT, and the next call
+    matches the oracle."""
+    from oracle import fusion
+    for HD in (0, 128):
+        x = synthetic.make_transition_inputs(1, 40, 128, 512, seed=8, HD=HD)
+        xd = {k: (None if v is None else v.to("cuda")) for k, v in x.items()}
+        run = lambda: evoattn.transition(xd["z"], xd["gamma"], xd["beta"], xd["w1"], xd["w2"],
+                                         o=xd["o"], w_o=xd["w_o"])
+        assert _stalled(run) == evoattn.ERR_TIMEOUT
+        out = run()
+        assert evoattn.device_status() == evoattn.OK
+        ref = fusion.transition(x["z"], x["gamma"], x["beta"], x["w1"], x["w2"], o=x["o"],
+                                w_o=x["w_o"])
+        assert rel_l2(out, ref) <= 5e-3
