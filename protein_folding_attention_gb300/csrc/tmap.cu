@@ -20,7 +20,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                     const uint64_t* byte_strides, const uint32_t* box,
-                    CUtensorMapSwizzle swizzle) {
+                    CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promotion) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t gdim[5], gstr[4];
@@ -33,7 +33,7 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t
   }
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
                    const_cast<void*>(base), gdim, gstr, bdim, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promotion,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
