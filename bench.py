@@ -135,12 +135,32 @@ PER_CONFIG = ("pairformer_start_n384", "pairformer_end_n768", "msa_row_s512_n384
               "long_start_n1536")
 
 
-def measure_config(w, dev, peak, steps=5, warmup=3):
+def algorithmic_bytes(w):
+    """HBM bytes the forward and the backward must move at least, the logits
+    never counted (they stay on chip): forward reads q, k, v, g, the pair
+    bias and the mask and writes out and lse; backward reads q, k, v, g, out
+    and dout, the pair bias, the mask, lse and delta, and writes dq, dk, dv,
+    dgate and dbias (fp32).  Returns (forward, backward)."""
+    L = w.B * w.S * w.H * w.N * w.D
+    R = w.B * w.S * w.H * w.N
+    n2 = w.B * w.H * w.N * w.N
+    e = 2 if w.dtype == "bf16" else 4
+    gl = 1 if w.gate else 0
+    mask = w.B * w.S * w.N if w.mask != "none" else 0
+    fwd = (3 + gl) * L * e + n2 * e + mask + L * e + R * 4
+    bwd = (5 + gl) * L * e + (3 + gl) * L * e + n2 * e + n2 * 4 + mask + 3 * R * 4
+    return fwd, bwd
+
+
+def measure_config(w, dev, peak, steps=5, warmup=3, hbm_peak=None, ex2_peak=None):
     """Forward and backward of one workload on its own inputs: CUDA-event
-    times (median over `steps`), TFLOP/s, fraction of the bf16 peak, and the
-    device bytes the caller holds for the call (inputs, outputs and the
-    backward workspace: the library allocates nothing itself).  Returns a
-    dict; every tensor it allocated is freed on return."""
+    times (median over `steps`), TFLOP/s, fraction of the bf16 peak, the
+    rate of the algorithmic HBM bytes against the measured copy bandwidth
+    (`hbm_peak`, GB/s), logits per second against the exponential unit
+    (`ex2_peak`, ex2/s; one ex2 per logit in each pass), and the device bytes
+    the caller holds for the call (inputs, outputs and the backward
+    workspace: the library allocates nothing itself).  Returns a dict; every
+    tensor it allocated is freed on return."""
     import torch
 
     from protein_folding_attention_gb300 import evoattn, synthetic
@@ -191,6 +211,15 @@ def measure_config(w, dev, peak, steps=5, warmup=3):
            "formula_bytes": held_bytes(B, S, H, N, D, gate=w.gate, mask=w.mask != "none"),
            "bwd_workspace_bytes": int(wsp.numel()),
            "logits_bytes_if_materialized_bf16": int(w.logits * 2)}
+    fb, bb = algorithmic_bytes(w)
+    res["fwd_hbm_bytes"], res["bwd_hbm_bytes"] = fb, bb
+    res["fwd_hbm_gbs"], res["bwd_hbm_gbs"] = fb / t_f / 1e9, bb / t_b / 1e9
+    if hbm_peak:
+        res["fwd_hbm_frac"] = fb / t_f / 1e9 / hbm_peak
+        res["bwd_hbm_frac"] = bb / t_b / 1e9 / hbm_peak
+    res["fwd_logits_per_s"], res["bwd_logits_per_s"] = w.logits / t_f, w.logits / t_b
+    if ex2_peak:
+        res["fwd_ex2_frac"] = w.logits / t_f / ex2_peak
     del x, out, lse, g, dbias, wsp
     torch.cuda.synchronize(dev)
     return res
@@ -654,8 +683,11 @@ def run_ours(args, w):
     per_config = None
     if rank == 0 and not args.no_per_config:
         per_config = {}
+        n_sm_cfg = torch.cuda.get_device_properties(dev).multi_processor_count
+        ex2_cfg = EX2_PER_CLK_PER_SM * n_sm_cfg * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
         for name in PER_CONFIG:
-            per_config[name] = measure_config(synthetic.WORKLOADS[name], dev, peak)
+            per_config[name] = measure_config(synthetic.WORKLOADS[name], dev, peak,
+                                              hbm_peak=peaks["hbm_gbs"], ex2_peak=ex2_cfg)
         per_config["memory_fit"] = memory_model()
     evofusion = None
     if rank == 0 and not args.no_per_config:

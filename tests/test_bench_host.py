@@ -105,3 +105,14 @@ def test_library_footprint_has_no_logit_term():
     assert f["bytes_per_BSN"] == pytest.approx(1.0)
     assert f["bytes_per_slot_partial"] == pytest.approx(4.0)
     assert abs(f["bytes_per_logit"]) < 1e-9
+
+
+def test_algorithmic_bytes_of_the_workloads():
+    """The HBM bytes each pass must move (logits never counted), per workload,
+    in MB: forward and backward of the four bf16 configurations."""
+    from protein_folding_attention_gb300 import synthetic
+    expect = {"pairformer_start_n384": (192.4, 388.3), "pairformer_end_n768": (769.7, 1553.0),
+              "msa_row_s512_n384": (512.2, 1032.8), "long_start_n1536": (3078.9, 6212.0)}
+    for name, (f, b) in expect.items():
+        fb, bb = bench.algorithmic_bytes(synthetic.WORKLOADS[name])
+        assert fb / 1e6 == pytest.approx(f, abs=0.1) and bb / 1e6 == pytest.approx(b, abs=0.1)
