@@ -166,8 +166,11 @@ def measure_config(w, dev, peak, steps=5, warmup=3, hbm_peak=None, ex2_peak=None
     from protein_folding_attention_gb300 import evoattn, synthetic
     torch.cuda.synchronize(dev)
     base = torch.cuda.memory_allocated(dev)
-    torch.cuda.reset_peak_memory_stats(dev)
     x = synthetic.make_inputs(w, device=dev)
+    # the input generator's own temporaries (e.g. the fp32 draw behind a
+    # Bernoulli mask) are not part of the call: count from here
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
     B, S, H, N, D = w.B, w.S, w.H, w.N, w.D
     out = synthetic.empty_view(w, dev)
     lse = torch.empty(B, S, H, N, device=dev, dtype=torch.float32)
