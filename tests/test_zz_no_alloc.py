@@ -107,6 +107,25 @@ def test_noalloc_atomic_dbias_twice():
         assert rel_l2(g["dq"], ref["dq"]) <= GRAD_REL
 
 
+def test_noalloc_deterministic_dq_bit_for_bit():
+    """With EVOATTN_DQ_DETERMINISTIC every gradient, dq included, is fixed by
+    the problem: the no-alloc entry point, after the scratch was dirtied by
+    another problem, must give the workspace call's bits for all five."""
+    fn = _noalloc_fn()
+    flags = evoattn.DBIAS_DETERMINISTIC | evoattn.DQ_DETERMINISTIC
+    x, out, lse = _problem("ending", S=12, N=200, seed=23)
+    assert evoattn.workspace_size(1, 12, 2, 200, 32, flags=flags) <= SCRATCH_BYTES
+    ref = evoattn.bwd(x["q"], x["k"], x["v"], x["bias"], x["mask"], x["gate"], out, lse,
+                      x["dout"], flags=flags)
+    ref = {k: v.clone() for k, v in ref.items()}
+    other, o_out, o_lse = _problem("starting", S=24, N=256, seed=7)
+    for _ in range(2):
+        _noalloc_grads(fn, other, o_out, o_lse, evoattn.DBIAS_ATOMIC)  # dirty scratch
+        g = _noalloc_grads(fn, x, out, lse, flags)
+        for n in ("dq", "dk", "dv", "dgate", "dbias"):
+            assert torch.equal(_bits(g[n]), _bits(ref[n])), n
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     w = synthetic.small("big", B=1, S=64, N=384, H=4, D=32, dtype="bf16", node="starting",
                         mask="none", gate=False, seed=1)
