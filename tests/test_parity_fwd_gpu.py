@@ -50,6 +50,31 @@ CASES = [
 ]
 
 
+# More work items (query tile x head x row group) than SMs, and S not a
+# multiple of the row group, so partial groups (fewer rows, one warpgroup
+# idle) sit between full ones in the same launch.
+MULTI_ITEM = [
+    # (S, N, H, D, node, mask, gate)
+    (7, 704, 16, 32, "ending", "bernoulli", True),     # 192 items, groups of 4 and 3
+    (5, 520, 16, 16, "starting", "tail", False),      # 160 items, groups of 4 and 1
+    (3, 640, 16, 64, "msa", "bernoulli", True),        # 160 items, groups of 2 and 1
+]
+
+
+@pytest.mark.parametrize("S,N,H,D,node,mask,gate", MULTI_ITEM)
+def test_bf16_fwd_many_items(S, N, H, D, node, mask, gate):
+    w = synthetic.small("mi", B=1, S=S, N=N, H=H, D=D, dtype="bf16", node=node, mask=mask,
+                        mask_tail=max(1, N // 10), mask_p=0.2, gate=gate, seed=S * 100 + N + D)
+    x = synthetic.make_inputs(w)
+    out, lse = run_fwd(x)
+    check_fwd(x, out, lse)
+    # the same call again gives the same bits (no state carried between
+    # launches)
+    out2, lse2 = run_fwd(x)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+
+
 @pytest.mark.parametrize("S,N,H,D,node,mask,gate", CASES)
 def test_bf16_fwd_small(S, N, H, D, node, mask, gate):
     w = synthetic.small("c", B=1, S=S, N=N, H=H, D=D, dtype="bf16", node=node, mask=mask,
