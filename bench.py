@@ -510,6 +510,16 @@ def run_ours(args, w):
     barrier()
     stage_a = [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev_a) * 1e-3
                for k in range(n_ev - 1)]
+    # and the fused mode: dbias summed with atomics inside the dK/dV pass
+    ev_z = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+            for _ in range(max(3, args.steps // 2))]
+    for _ in range(2):
+        bwd(None, evoattn.DBIAS_FUSED)
+    for e in ev_z:
+        bwd(e, evoattn.DBIAS_FUSED)
+    barrier()
+    stage_z = [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev_z) * 1e-3
+               for k in range(n_ev - 1)]
     # HBM bytes of the deterministic reduce stage: slot partials read + dbias
     # written (k_dbias_sum), fp32 dQ read + bf16 dq written (k_dq_convert)
     nt = (w.N + 127) // 128
@@ -523,6 +533,8 @@ def run_ours(args, w):
                           "reduce_hbm_gbs": reduce_bytes / stage[3] / 1e9},
         "atomic": {"dbias_ms": stage_a[2] * 1e3, "reduce_ms": stage_a[3] * 1e3,
                    "bwd_ms": sum(stage_a) * 1e3},
+        "fused": {"dkdv_with_dbias_ms": stage_z[1] * 1e3, "reduce_ms": stage_z[3] * 1e3,
+                  "bwd_ms": sum(stage_z) * 1e3},
     }
 
     # ---- dQ: the deterministic mode (per-key-tile slices, ordered sum) timed

@@ -97,6 +97,7 @@ typedef enum { EVOATTN_BF16 = 0, EVOATTN_F32 = 1 } evoattn_dtype;
 #define EVOATTN_DBIAS_DETERMINISTIC 0u  /* fixed s-slots + ordered sum: bit-identical */
 #define EVOATTN_DBIAS_ATOMIC 1u         /* s-slot partials added with fp32 atomics */
 #define EVOATTN_DQ_DETERMINISTIC 2u     /* per-key-tile dQ slices + ordered sum */
+#define EVOATTN_DBIAS_FUSED 4u          /* dbias summed in the dK/dV pass (fp32 atomics) */
 
 /*
  * Forward (MegaFold technical summary, "Methodik" section 1 "EvoFlash-3D",
@@ -157,10 +158,16 @@ size_t evoattn_bwd_workspace_size(int B, int S, int H, int N, int D,
  *                             stores its partial into a slice of its own
  *                             and the slices are summed in key-tile order
  *                             (workspace: ceil(N/128) fp32 copies of dq
- *                             instead of one).  dk, dv and dgate are
- *                             bit-identical in every mode; the F32 path is
- *                             deterministic whatever the flags.  Other bits
- *                             set: EVOATTN_ERR_INVALID_ARG.
+ *                             instead of one).  EVOATTN_DBIAS_FUSED (BF16;
+ *                             it overrides the two dbias modes above) adds
+ *                             every logit gradient into dbias with fp32
+ *                             atomics from the pass that computes dK and dV,
+ *                             so the logits are recomputed once instead of
+ *                             twice; order-dependent rounding, no slot
+ *                             partials in the workspace.  dk, dv and dgate
+ *                             are bit-identical in every mode; the F32 path
+ *                             is deterministic whatever the flags.  Other
+ *                             bits set: EVOATTN_ERR_INVALID_ARG.
  *  workspace                : device, 256-byte aligned, at least
  *                             evoattn_bwd_workspace_size(...) bytes; the
  *                             library overwrites it; it must not be used by

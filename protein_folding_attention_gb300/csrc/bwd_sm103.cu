@@ -83,7 +83,7 @@ Workspace carve(const Problem& P, unsigned flags, void* base) {
   w.dq_acc = reinterpret_cast<float*>(b + off);
   off = align256(off + (size_t)w.dq_slices * L * 4);
   w.partial = reinterpret_cast<float*>(b + off);
-  if (!(flags & EVOATTN_DBIAS_ATOMIC))
+  if (!(flags & (EVOATTN_DBIAS_ATOMIC | EVOATTN_DBIAS_FUSED)))
     off = align256(off + (size_t)dbias_slots(P) * P.B * P.H * P.N * P.N * 4);
   w.bytes = off;
   return w;
@@ -303,6 +303,7 @@ struct DkdvParams {
   int64_t dq_slice;
   __nv_bfloat16 *dk, *dv;
   Strides5 sdk, sdv;
+  float* dbias;  // fused dbias: dense fp32 [B,H,N,N], zeroed before the launch
   WaitCfg wc;
 };
 
@@ -311,7 +312,9 @@ struct DkdvItem {
   int64_t row0;  // row of (b, s, h, 0) in a dense [B,S,H,N] array
 };
 
-template <int D, bool BIAS_K_CONTIG>
+// FUSED_DBIAS: the logit gradients are also added into dbias (fp32 atomics)
+// here, so no second pass recomputes them.
+template <int D, bool BIAS_K_CONTIG, bool FUSED_DBIAS>
 __global__ void __launch_bounds__(384, 1)
     k_dkdv(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -634,6 +637,7 @@ __global__ void __launch_bounds__(384, 1)
     const float inv_sqrt_d = rsqrtf((float)D);
     const float2 c1c1 = make_float2(c1, c1), l2l2 = make_float2(kLog2e, kLog2e),
                  isd = make_float2(inv_sqrt_d, inv_sqrt_d);
+    const float sqrt_d = sqrtf((float)D);
     // dQ partial of tile t (query tile jt_t of the item at row0_t, key tile
     // kt_t): lane = query; this warpgroup adds (or, deterministic, stores)
     // half of D
@@ -711,6 +715,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int n = 0; n < my_items && ok; ++n) {
       const DkdvItem it = item(n);
       const int kg = it.kt * 128 + kl;  // key index
+      float* const dbias_row =
+          FUSED_DBIAS ? p.dbias + ((int64_t)it.b * p.H + it.h) * p.N * p.N : nullptr;
       // additive mask of this key, log2 units (constant over the query tiles)
       float madd = 0.f;
       if (kg >= p.N) madd = -INFINITY;
@@ -758,6 +764,16 @@ __global__ void __launch_bounds__(384, 1)
             const float2 ds = mul2(pr, gg);
             pk[4 * c + e] = pack_bf16(pr.x, pr.y);
             dk2[4 * c + e] = pack_bf16(ds.x, ds.y);
+            if constexpr (FUSED_DBIAS) {
+              // dbias[b, h, j, k] += the logit gradient (ds carries the
+              // 1/sqrt(D) of dQ and dK); a warp covers 32 consecutive keys
+              const int jq = jt * 128 + 64 * wg + j2;
+              if (kg < p.N) {
+                float* cell = dbias_row + (int64_t)jq * p.N + kg;
+                if (jq < p.N) atomicAdd(cell, ds.x * sqrt_d);
+                if (jq + 1 < p.N) atomicAdd(cell + p.N, ds.y * sqrt_d);
+              }
+            }
           }
         }
         // the previous tile's MMAs read P^T, dS^T and the dS tile: wait for them
@@ -1290,7 +1306,8 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     const int64_t units = P.rows() * (D / 8);
     k_pre<D, U><<<(unsigned)((units + 256 * U - 1) / (256 * U)), 256, 0, st>>>(pp);
   }
-  if (flags & EVOATTN_DBIAS_ATOMIC) {
+  const bool fused = (flags & EVOATTN_DBIAS_FUSED) != 0;
+  if (fused || (flags & EVOATTN_DBIAS_ATOMIC)) {
     cudaError_t e = cudaMemsetAsync(a.dbias, 0, (size_t)P.B * P.H * P.N * P.N * 4, st);
     if (e != cudaSuccess) return e;
   }
@@ -1309,7 +1326,8 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     dp.dq_slice = P.rows() * D;
     dp.dk = static_cast<__nv_bfloat16*>(a.dk); dp.dv = static_cast<__nv_bfloat16*>(a.dv);
     dp.sdk = P.dk; dp.sdv = P.dv; dp.wc = launch_wait(wait);
-    auto kern = k_dkdv<D, KC>;
+    dp.dbias = static_cast<float*>(a.dbias);
+    auto kern = fused ? k_dkdv<D, KC, true> : k_dkdv<D, KC, false>;
     cudaError_t e = set_smem(kern, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     e = check_regs(kern, C::LAUNCH_REGS);
@@ -1323,9 +1341,9 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
     kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, tb, dp);
   }
   if (ev) cudaEventRecord(ev[2], st);
-  // 3) dbias partials
+  // 3) dbias partials (none when dbias was summed in step 2)
   const int slots = dbias_slots(P);
-  {
+  if (!fused) {
     using C = DbiasCfg<D>;
     DbiasParams bp{};
     bp.B = P.B; bp.S = P.S; bp.H = P.H; bp.N = P.N; bp.njt = nt; bp.nkt = nt;
@@ -1346,7 +1364,7 @@ cudaError_t bwd_launch(const Problem& P, const Bf16Ptrs& a, unsigned flags, cons
   }
   if (ev) cudaEventRecord(ev[3], st);
   // 4) ordered slot sum, dQ conversion
-  if (!(flags & EVOATTN_DBIAS_ATOMIC)) {
+  if (!fused && !(flags & EVOATTN_DBIAS_ATOMIC)) {
     const int64_t n = (int64_t)P.B * P.H * P.N * P.N;
     const int64_t work = (n & 3) == 0 ? n / 4 : n;
     k_dbias_sum<<<(unsigned)((work + 255) / 256), 256, 0, st>>>(w.partial, a.dbias, n, slots);

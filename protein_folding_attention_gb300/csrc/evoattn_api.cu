@@ -254,7 +254,7 @@ evoattn_status evoattn_fwd(const void* q, const int64_t q_strides[5], const void
 
 size_t evoattn_bwd_workspace_size(int B, int S, int H, int N, int D, evoattn_dtype dtype,
                                   unsigned flags) {
-  if (B < 1 || S < 1 || H < 1 || N < 1 || !d_supported_bwd(dtype, D) || (flags & ~3u)) return 0;
+  if (B < 1 || S < 1 || H < 1 || N < 1 || !d_supported_bwd(dtype, D) || (flags & ~7u)) return 0;
   Problem P{};
   P.B = B; P.S = S; P.H = H; P.N = N; P.D = D;
   return dtype == EVOATTN_F32 ? f32_bwd_workspace_bytes(P) : bf16_bwd_workspace_bytes(P, flags);
@@ -283,7 +283,7 @@ static evoattn_status bwd_impl(const void* q, const int64_t q_strides[5], const 
   if ((gate == nullptr) != (dgate == nullptr)) return EVOATTN_ERR_INVALID_ARG;
   if (dgate && !dgate_strides) return EVOATTN_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || H < 1 || N < 1 || D < 1) return EVOATTN_ERR_INVALID_ARG;
-  if (flags & ~3u) return EVOATTN_ERR_INVALID_ARG;
+  if (flags & ~7u) return EVOATTN_ERR_INVALID_ARG;
   if (dtype != EVOATTN_BF16 && dtype != EVOATTN_F32) return EVOATTN_ERR_UNSUPPORTED;
   if (!d_supported_bwd(dtype, D)) return EVOATTN_ERR_UNSUPPORTED;
   if (!nonneg(q_strides, 5) || !nonneg(k_strides, 5) || !nonneg(v_strides, 5) ||

@@ -20,6 +20,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, ER
 BF16, F32 = 0, 1
 DBIAS_DETERMINISTIC, DBIAS_ATOMIC = 0, 1
 DQ_DETERMINISTIC = 2  # OR-ed with either: dq bit-identical too
+DBIAS_FUSED = 4  # dbias summed in the dK/dV pass (fp32 atomics)
 
 _lib = None
 _I64_5 = ctypes.c_int64 * 5

@@ -106,8 +106,8 @@ def test_bwd_rejects_bad_arguments(lib):
     assert call_bwd(lib, dq=None) == evoattn.ERR_INVALID_ARG
     assert call_bwd(lib, gate=FAKE, dgate=None) == evoattn.ERR_INVALID_ARG
     assert call_bwd(lib, gate=None, dgate=FAKE) == evoattn.ERR_INVALID_ARG
-    assert call_bwd(lib, flags=4) == evoattn.ERR_INVALID_ARG
-    assert call_bwd(lib, flags=6) == evoattn.ERR_INVALID_ARG
+    assert call_bwd(lib, flags=8) == evoattn.ERR_INVALID_ARG
+    assert call_bwd(lib, flags=14) == evoattn.ERR_INVALID_ARG
     assert call_bwd(lib, ws=None) == evoattn.ERR_WORKSPACE
     assert call_bwd(lib, ws_bytes=16) == evoattn.ERR_WORKSPACE
     assert call_bwd(lib, ws=ctypes.c_void_p((1 << 20) + 16)) == evoattn.ERR_WORKSPACE
@@ -141,6 +141,18 @@ def test_bf16_backward_d64_is_unsupported(lib):
     assert call_fwd(lib, shape=shape, q=ctypes.c_void_p((1 << 20) + 8)) == evoattn.ERR_ALIGNMENT
 
 
+def test_fused_dbias_workspace(lib):
+    """EVOATTN_DBIAS_FUSED keeps no slot partials: its workspace equals the
+    atomic mode's (both modes of dQ), below the deterministic mode's."""
+    B, S, H, N, D = 1, 8, 2, 300, 32
+    for dq in (0, evoattn.DQ_DETERMINISTIC):
+        fused = evoattn.workspace_size(B, S, H, N, D, flags=evoattn.DBIAS_FUSED | dq)
+        assert fused == evoattn.workspace_size(B, S, H, N, D, flags=evoattn.DBIAS_ATOMIC | dq)
+        assert fused < evoattn.workspace_size(B, S, H, N, D, flags=dq)
+        assert fused == evoattn.workspace_size(
+            B, S, H, N, D, flags=evoattn.DBIAS_FUSED | evoattn.DBIAS_ATOMIC | dq)
+
+
 def test_deterministic_dq_workspace(lib):
     """EVOATTN_DQ_DETERMINISTIC combines with either dbias mode; its BF16
     workspace holds one fp32 dQ slice per 128-key tile instead of one, the
@@ -159,7 +171,7 @@ def test_deterministic_dq_workspace(lib):
     f32 = torch_f32()
     assert evoattn.workspace_size(B, S, H, N, D, f32, flags=evoattn.DQ_DETERMINISTIC) == \
         evoattn.workspace_size(B, S, H, N, D, f32)
-    assert evoattn.workspace_size(B, S, H, N, D, flags=4) == 0
+    assert evoattn.workspace_size(B, S, H, N, D, flags=8) == 0
     assert call_bwd_noalloc(lib, flags=8) == evoattn.ERR_INVALID_ARG
 
 

@@ -64,7 +64,8 @@ CASES = [
 
 
 @pytest.mark.parametrize("S,N,H,D,node,mask,gate", CASES)
-@pytest.mark.parametrize("flags", [evoattn.DBIAS_DETERMINISTIC, evoattn.DBIAS_ATOMIC])
+@pytest.mark.parametrize("flags", [evoattn.DBIAS_DETERMINISTIC, evoattn.DBIAS_ATOMIC,
+                                   evoattn.DBIAS_FUSED])
 def test_bf16_bwd_small(S, N, H, D, node, mask, gate, flags):
     w = synthetic.small("c", B=1, S=S, N=N, H=H, D=D, dtype="bf16", node=node, mask=mask,
                         mask_tail=max(1, N // 10), mask_p=0.2, gate=gate, seed=S * 1000 + N + 7)
@@ -156,6 +157,28 @@ def test_bf16_bwd_full_size_every_row_end_n768():
 
 def test_bf16_bwd_full_size_every_row_atomic_dbias():
     _full_size_all_rows("pairformer_start_n384", evoattn.DBIAS_ATOMIC)
+
+
+def test_bf16_bwd_full_size_every_row_fused_dbias():
+    """dbias summed inside the dK/dV pass: the MSA-row workload (S = 512,
+    three key tiles, Bernoulli key mask), every gradient over every s row."""
+    _full_size_all_rows("msa_row_s512_n384", evoattn.DBIAS_FUSED)
+
+
+def test_fused_dbias_leaves_the_other_gradients_unchanged():
+    """The fused mode only adds the dbias atomics to the dK/dV pass: dk, dv
+    and dgate are the default mode's bits, dq differs by the order of its
+    fp32 additions at most, and dbias agrees with the deterministic sum to
+    fp32 reordering."""
+    w = synthetic.small("fz", B=1, S=10, N=296, H=2, D=32, dtype="bf16", node="ending",
+                        mask="bernoulli", mask_p=0.2, gate=True, seed=123)
+    x = synthetic.make_inputs(w)
+    a = run_fwd_bwd(x)
+    b = run_fwd_bwd(x, evoattn.DBIAS_FUSED)
+    for k in ("dk", "dv", "dgate"):
+        assert torch.equal(a[k].view(torch.int16), b[k].view(torch.int16)), k
+    assert rel_l2(b["dq"], a["dq"]) < 2e-3
+    assert rel_l2(b["dbias"], a["dbias"]) < 1e-4
 
 
 @pytest.mark.parametrize("name", ["pairformer_start_n384", "pairformer_end_n768",
