@@ -49,7 +49,8 @@ def test_forward_gives_up_and_recovers(node):
     assert rel_l2(lse, ref_lse) <= FWD_REL
 
 
-@pytest.mark.parametrize("flags", [evoattn.DBIAS_DETERMINISTIC, evoattn.DBIAS_ATOMIC])
+@pytest.mark.parametrize("flags", [evoattn.DBIAS_DETERMINISTIC, evoattn.DBIAS_ATOMIC,
+                                   evoattn.DBIAS_FUSED])
 def test_backward_gives_up_and_recovers(flags):
     x, xd = _inputs("ending")
     args = (xd["q"], xd["k"], xd["v"], xd["bias"], xd["mask"], xd["gate"])
